@@ -1,0 +1,347 @@
+// C ABI of libfp8bw (declared in include/fp8bw.h): argument validation, the
+// per-device error word, and dispatch to the kernel launchers.  Nothing here
+// computes on the host; every call ends in a kernel launch or an error code.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "fp8bw.h"
+#include "launch.h"
+
+#define FP8BW_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+thread_local char g_msg[512];
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  g_msg[0] = '\0';
+  return FP8BW_OK;
+}
+
+// The device error word: set by kernels when a bounded wait expires or a
+// device-side argument check fails; read and cleared by fp8bw_sync_status.
+__device__ int g_error_word;
+
+struct DeviceState {
+  bool probed = false;
+  bool supported = false;
+  int num_sms = 0;
+  int* error_word = nullptr;
+  char why[160] = {0};
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+// Checks (once per device) that the current device is compute capability
+// 10.3 and resolves the address of its error word.
+int current_device(DeviceState** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return fail(FP8BW_ERR_UNSUPPORTED, "no usable CUDA device (%s)", cudaGetErrorString(e));
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.probed) {
+    d.probed = true;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (major != 10 || minor != 3) {
+      snprintf(d.why, sizeof(d.why), "device %d has compute capability %d.%d; the kernels are built for sm_103a", dev,
+               major, minor);
+    } else {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_error_word);
+      if (e != cudaSuccess) {
+        snprintf(d.why, sizeof(d.why), "cannot resolve the error word: %s", cudaGetErrorString(e));
+        cudaGetLastError();
+      } else {
+        d.error_word = static_cast<int*>(p);
+        d.supported = true;
+      }
+    }
+  }
+  if (!d.supported) return fail(FP8BW_ERR_UNSUPPORTED, "%s", d.why);
+  *out = &d;
+  return FP8BW_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
+
+bool dim_ok(int64_t d, int64_t mult) { return d > 0 && d <= kMaxDim && d % mult == 0; }
+
+bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + static_cast<uintptr_t>(bbytes) && b0 < a0 + static_cast<uintptr_t>(abytes);
+}
+
+int launched(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(FP8BW_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+  return ok();
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+namespace fp8bw {
+
+void* tensor_map_encoder() {
+  static void* fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = p;
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+}  // namespace fp8bw
+
+// ============================================================ quantizers
+
+FP8BW_API int fp8bw_quant_1x128_row(const fp8bw_bf16* x, int64_t R, int64_t C, uint8_t* q, float* s, void* stream) {
+  if (!x || !q || !s) return fail(FP8BW_ERR_NULL, "fp8bw_quant_1x128_row: x, q and s must be non-NULL");
+  if (!dim_ok(R, 128) || !dim_ok(C, 128) || R / 128 > 65535)
+    return fail(FP8BW_ERR_SHAPE, "fp8bw_quant_1x128_row: R=%lld and C=%lld must be positive multiples of 128",
+                (long long)R, (long long)C);
+  if (!aligned16(x) || !aligned16(q) || !aligned16(s))
+    return fail(FP8BW_ERR_ALIGN, "fp8bw_quant_1x128_row: pointers must be 16-byte aligned");
+  if (overlaps(x, R * C * 2, q, R * C) || overlaps(x, R * C * 2, s, C / 128 * R * 4))
+    return fail(FP8BW_ERR_LAYOUT, "fp8bw_quant_1x128_row: outputs overlap the input");
+  DeviceState* d;
+  if (int rc = current_device(&d)) return rc;
+  return launched(fp8bw::launch_quant_1x128_row(x, R, C, q, s, as_stream(stream)), "fp8bw_quant_1x128_row");
+}
+
+FP8BW_API int fp8bw_quant_1x128_col(const fp8bw_bf16* x, int64_t R, int64_t C, uint8_t* qT, float* s, void* stream) {
+  if (!x || !qT || !s) return fail(FP8BW_ERR_NULL, "fp8bw_quant_1x128_col: x, qT and s must be non-NULL");
+  if (!dim_ok(R, 128) || !dim_ok(C, 128) || R / 128 > 65535)
+    return fail(FP8BW_ERR_SHAPE, "fp8bw_quant_1x128_col: R=%lld and C=%lld must be positive multiples of 128",
+                (long long)R, (long long)C);
+  if (!aligned16(x) || !aligned16(qT) || !aligned16(s))
+    return fail(FP8BW_ERR_ALIGN, "fp8bw_quant_1x128_col: pointers must be 16-byte aligned");
+  if (overlaps(x, R * C * 2, qT, R * C) || overlaps(x, R * C * 2, s, R / 128 * C * 4))
+    return fail(FP8BW_ERR_LAYOUT, "fp8bw_quant_1x128_col: outputs overlap the input");
+  DeviceState* d;
+  if (int rc = current_device(&d)) return rc;
+  return launched(fp8bw::launch_quant_1x128_col(x, R, C, qT, s, as_stream(stream)), "fp8bw_quant_1x128_col");
+}
+
+FP8BW_API int fp8bw_quant_128x128(const fp8bw_bf16* w, int64_t R, int64_t C, uint8_t* q, uint8_t* qT, float* s,
+                                  void* stream) {
+  if (!w || !q || !s) return fail(FP8BW_ERR_NULL, "fp8bw_quant_128x128: w, q and s must be non-NULL");
+  if (!dim_ok(R, 128) || !dim_ok(C, 128) || R / 128 > 65535)
+    return fail(FP8BW_ERR_SHAPE, "fp8bw_quant_128x128: R=%lld and C=%lld must be positive multiples of 128",
+                (long long)R, (long long)C);
+  if (!aligned16(w) || !aligned16(q) || !aligned16(s) || (qT && !aligned16(qT)))
+    return fail(FP8BW_ERR_ALIGN, "fp8bw_quant_128x128: pointers must be 16-byte aligned");
+  const int64_t ld = FP8BW_SCALE_LD_128X128(C);
+  if (overlaps(w, R * C * 2, q, R * C) || (qT && overlaps(w, R * C * 2, qT, R * C)) ||
+      overlaps(w, R * C * 2, s, R / 128 * ld * 4) || (qT && overlaps(q, R * C, qT, R * C)))
+    return fail(FP8BW_ERR_LAYOUT, "fp8bw_quant_128x128: outputs overlap the input or each other");
+  DeviceState* d;
+  if (int rc = current_device(&d)) return rc;
+  return launched(fp8bw::launch_quant_128x128(w, R, C, q, qT, s, ld, as_stream(stream)), "fp8bw_quant_128x128");
+}
+
+FP8BW_API int mxfp8_quant_1x32_row(const fp8bw_bf16* x, int64_t R, int64_t C, uint8_t* q, uint8_t* e8, int mode,
+                                   void* stream) {
+  if (!x || !q || !e8) return fail(FP8BW_ERR_NULL, "mxfp8_quant_1x32_row: x, q and e8 must be non-NULL");
+  if (!dim_ok(R, 1) || !dim_ok(C, 32) || (R + 31) / 32 > 65535)
+    return fail(FP8BW_ERR_SHAPE, "mxfp8_quant_1x32_row: R=%lld must be positive, C=%lld a positive multiple of 32",
+                (long long)R, (long long)C);
+  if (!aligned16(x) || !aligned16(q) || !aligned16(e8))
+    return fail(FP8BW_ERR_ALIGN, "mxfp8_quant_1x32_row: pointers must be 16-byte aligned");
+  if (mode != FP8BW_MX_RCEIL && mode != FP8BW_MX_FLOOR)
+    return fail(FP8BW_ERR_ARG, "mxfp8_quant_1x32_row: mode %d is neither RCEIL (0) nor FLOOR (1)", mode);
+  if (overlaps(x, R * C * 2, q, R * C) || overlaps(x, R * C * 2, e8, R * C / 32))
+    return fail(FP8BW_ERR_LAYOUT, "mxfp8_quant_1x32_row: outputs overlap the input");
+  DeviceState* d;
+  if (int rc = current_device(&d)) return rc;
+  return launched(fp8bw::launch_mx_quant_row(x, R, C, q, e8, mode, as_stream(stream)), "mxfp8_quant_1x32_row");
+}
+
+static int mx_col_common(const char* name, const fp8bw_bf16* x, int64_t G, int64_t R, int64_t C, uint8_t* qT,
+                         uint8_t* e8, int mode, void* stream) {
+  if (!x || !qT || !e8) return fail(FP8BW_ERR_NULL, "%s: input, qT and e8 must be non-NULL", name);
+  if (!dim_ok(G, 1) || G > 65535 || !dim_ok(R, 32) || !dim_ok(C, 8) || (R + 127) / 128 > 65535)
+    return fail(FP8BW_ERR_SHAPE, "%s: the blocked dim (%lld) must be a positive multiple of 32, the other (%lld) of 8",
+                name, (long long)R, (long long)C);
+  if (!aligned16(x) || !aligned16(qT) || !aligned16(e8))
+    return fail(FP8BW_ERR_ALIGN, "%s: pointers must be 16-byte aligned", name);
+  if (mode != FP8BW_MX_RCEIL && mode != FP8BW_MX_FLOOR)
+    return fail(FP8BW_ERR_ARG, "%s: mode %d is neither RCEIL (0) nor FLOOR (1)", name, mode);
+  const int64_t n = G * R * C;
+  if (overlaps(x, n * 2, qT, n) || overlaps(x, n * 2, e8, n / 32))
+    return fail(FP8BW_ERR_LAYOUT, "%s: outputs overlap the input", name);
+  DeviceState* d;
+  if (int rc = current_device(&d)) return rc;
+  return launched(fp8bw::launch_mx_quant_col(x, G, R, C, qT, e8, mode, as_stream(stream)), name);
+}
+
+FP8BW_API int mxfp8_quant_1x32_col(const fp8bw_bf16* x, int64_t R, int64_t C, uint8_t* qT, uint8_t* e8, int mode,
+                                   void* stream) {
+  return mx_col_common("mxfp8_quant_1x32_col", x, 1, R, C, qT, e8, mode, stream);
+}
+
+FP8BW_API int mxfp8_quant_3d_col(const fp8bw_bf16* w, int64_t G, int64_t N, int64_t K, uint8_t* qT, uint8_t* e8,
+                                 int mode, void* stream) {
+  return mx_col_common("mxfp8_quant_3d_col", w, G, N, K, qT, e8, mode, stream);
+}
+
+// ============================================================ blockwise GEMMs
+
+static int gemm_common(const char* name, fp8bw::BlockwiseGemmArgs& g, void* stream) {
+  if (!g.a || !g.b || !g.sa || !g.sb || !g.out)
+    return fail(FP8BW_ERR_NULL, "%s: every operand, scale and output pointer must be non-NULL", name);
+  if (!dim_ok(g.Mo, 128) || !dim_ok(g.No, 256) || !dim_ok(g.Kc, 128))
+    return fail(FP8BW_ERR_SHAPE,
+                "%s: output rows (%lld) and the contraction (%lld) must be positive multiples of 128, output columns "
+                "(%lld) of 256",
+                name, (long long)g.Mo, (long long)g.Kc, (long long)g.No);
+  if (!aligned16(g.a) || !aligned16(g.b) || !aligned16(g.sa) || !aligned16(g.sb) || !aligned16(g.out))
+    return fail(FP8BW_ERR_ALIGN, "%s: pointers must be 16-byte aligned", name);
+  if (overlaps(g.out, g.Mo * g.No * 2, g.a, g.Mo * g.Kc) || overlaps(g.out, g.Mo * g.No * 2, g.b, g.No * g.Kc))
+    return fail(FP8BW_ERR_LAYOUT, "%s: the output overlaps an operand", name);
+  DeviceState* d;
+  if (int rc = current_device(&d)) return rc;
+  if (!fp8bw::tensor_map_encoder()) return fail(FP8BW_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", name);
+  g.status = d->error_word;
+  g.num_sms = d->num_sms;
+  return launched(fp8bw::launch_blockwise_gemm(g, as_stream(stream)), name);
+}
+
+FP8BW_API int fp8bw_gemm_fwd(const uint8_t* xq, const float* xs, const uint8_t* wq, const float* ws, fp8bw_bf16* y,
+                             int64_t M, int64_t N, int64_t K, void* stream) {
+  fp8bw::BlockwiseGemmArgs g{};
+  g.a = xq;
+  g.b = wq;
+  g.sa = xs;
+  g.sa_ld = M;
+  g.sb = ws;
+  g.sb_ld_nb = FP8BW_SCALE_LD_128X128(K);
+  g.sb_ld_kb = 1;
+  g.b_scale = fp8bw::BScale::kBlock128x128;
+  g.out = y;
+  g.Mo = M;
+  g.No = N;
+  g.Kc = K;
+  return gemm_common("fp8bw_gemm_fwd", g, stream);
+}
+
+FP8BW_API int fp8bw_gemm_dgrad(const uint8_t* dyq, const float* dys, const uint8_t* wqT, const float* ws,
+                               fp8bw_bf16* dx, int64_t M, int64_t N, int64_t K, void* stream) {
+  fp8bw::BlockwiseGemmArgs g{};
+  g.a = dyq;
+  g.b = wqT;
+  g.sa = dys;
+  g.sa_ld = M;
+  g.sb = ws;
+  g.sb_ld_nb = 1;                          // B rows are k: block k/128 is the column of ws
+  g.sb_ld_kb = FP8BW_SCALE_LD_128X128(K);  // contraction block n/128 is the row of ws
+  g.b_scale = fp8bw::BScale::kBlock128x128;
+  g.out = dx;
+  g.Mo = M;
+  g.No = K;
+  g.Kc = N;
+  return gemm_common("fp8bw_gemm_dgrad", g, stream);
+}
+
+FP8BW_API int fp8bw_gemm_wgrad(const uint8_t* dyqT, const float* dysT, const uint8_t* xqT, const float* xsT,
+                               fp8bw_bf16* dW, int64_t M, int64_t N, int64_t K, void* stream) {
+  fp8bw::BlockwiseGemmArgs g{};
+  g.a = dyqT;
+  g.b = xqT;
+  g.sa = dysT;
+  g.sa_ld = N;
+  g.sb = xsT;
+  g.sb_ld_nb = 0;
+  g.sb_ld_kb = K;
+  g.b_scale = fp8bw::BScale::kPerRow;
+  g.out = dW;
+  g.Mo = N;
+  g.No = K;
+  g.Kc = M;
+  return gemm_common("fp8bw_gemm_wgrad", g, stream);
+}
+
+// ============================================================ MXFP8 grouped GEMM
+
+FP8BW_API int mxfp8_grouped_gemm(int kind, const uint8_t* a, const uint8_t* a_e8, const uint8_t* b,
+                                 const uint8_t* b_e8, const int32_t* group_end, int64_t G, int64_t M, int64_t N,
+                                 int64_t K, fp8bw_bf16* out, void* stream) {
+  const char* name = "mxfp8_grouped_gemm";
+  if (!a || !a_e8 || !b || !b_e8 || !group_end || !out)
+    return fail(FP8BW_ERR_NULL, "%s: every operand, scale, group_end and output pointer must be non-NULL", name);
+  if (kind < FP8BW_GROUPED_FWD || kind > FP8BW_GROUPED_WGRAD)
+    return fail(FP8BW_ERR_ARG, "%s: kind %d is not FWD (0), DGRAD (1) or WGRAD (2)", name, kind);
+  const int64_t out_cols = kind == FP8BW_GROUPED_FWD ? N : K;
+  if (!dim_ok(G, 1) || G > 1024 || !dim_ok(M, 32) || !dim_ok(N, 128) || !dim_ok(K, 128) || out_cols % 256 != 0)
+    return fail(FP8BW_ERR_SHAPE,
+                "%s: need 0 < G <= 1024, M a multiple of 32, N and K multiples of 128 and the output column count "
+                "(%lld) a multiple of 256",
+                name, (long long)out_cols);
+  if (!aligned16(a) || !aligned16(a_e8) || !aligned16(b) || !aligned16(b_e8) || !aligned16(group_end) ||
+      !aligned16(out))
+    return fail(FP8BW_ERR_ALIGN, "%s: pointers must be 16-byte aligned", name);
+  DeviceState* d;
+  if (int rc = current_device(&d)) return rc;
+  if (!fp8bw::tensor_map_encoder()) return fail(FP8BW_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", name);
+  fp8bw::MxGroupedGemmArgs g{kind, a, a_e8, b, b_e8, group_end, G, M, N, K, out, d->error_word, d->num_sms};
+  return launched(fp8bw::launch_mx_grouped_gemm(g, as_stream(stream)), name);
+}
+
+// ============================================================ status
+
+FP8BW_API int fp8bw_sync_status(void* stream) {
+  DeviceState* d;
+  if (int rc = current_device(&d)) return rc;
+  cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+  if (e != cudaSuccess) return fail(FP8BW_ERR_CUDA, "fp8bw_sync_status: %s", cudaGetErrorString(e));
+  int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(int));
+  if (e != cudaSuccess) return fail(FP8BW_ERR_CUDA, "fp8bw_sync_status: reading the error word: %s", cudaGetErrorString(e));
+  if (word != 0) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));
+    if (word == FP8BW_ERR_TIMEOUT) return fail(FP8BW_ERR_TIMEOUT, "a bounded device-side wait expired");
+    return fail(word, "a kernel reported error %d (a device-side argument check failed)", word);
+  }
+  return ok();
+}
+
+FP8BW_API const char* fp8bw_last_error(void) { return g_msg; }
+
+FP8BW_API int fp8bw_selftest_bounded_wait(uint32_t timeout_us, void* stream) {
+  if (timeout_us < 1 || timeout_us > 2000000)
+    return fail(FP8BW_ERR_ARG, "fp8bw_selftest_bounded_wait: timeout_us=%u outside [1, 2000000]", timeout_us);
+  DeviceState* d;
+  if (int rc = current_device(&d)) return rc;
+  return launched(fp8bw::launch_selftest_bounded_wait(timeout_us, d->error_word, as_stream(stream)),
+                  "fp8bw_selftest_bounded_wait");
+}

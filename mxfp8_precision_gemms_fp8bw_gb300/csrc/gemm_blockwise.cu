@@ -1,0 +1,380 @@
+// Blockwise-scaled e4m3 GEMM on the 5th-generation tensor cores (tcgen05),
+// the three GEMMs of Float8BlockwiseLinear (PR #2386 description; PR #4295
+// Summary):
+//
+//   out[i, j] = sum_kb  sa[kb][i] * sb(kb, j) * P_kb[i, j],
+//   P_kb[i, j] = sum_{k in block kb} dec(A[i, k]) * dec(B[j, k])
+//
+// where kb runs over 128-deep contraction blocks.  The per-block scales are
+// arbitrary fp32 values (amax / 448), so they cannot ride on the tensor
+// core's power-of-two block scaling; instead each P_kb is accumulated by the
+// tensor core into tensor memory (TMEM) and "promoted" by CUDA cores into
+// fp32 register accumulators: acc += P_kb * sa * sb.
+//
+// Kernel structure (one persistent CTA per SM, 320 threads):
+//   warp 0      TMA producer: A tile 128x128 and B tile 256x128 (e4m3,
+//               128-byte swizzle) per contraction block into a 4-stage ring.
+//   warp 1      allocates / frees the 512 TMEM columns; one thread issues 4
+//               tcgen05.mma (K = 32 each) per block into one of two 128x256
+//               fp32 TMEM partial buffers, then commits to the smem ring's
+//               "empty" barrier and to the buffer's "full" barrier.
+//   warps 2-9   promotion + epilogue: warp w reads TMEM lanes 32*(w%4)...,
+//               warps 2-5 columns 0-127 and warps 6-9 columns 128-255 of the
+//               partial, multiply-add it into 128 fp32 accumulators per
+//               thread, release the buffer, and after the last block write
+//               their row of the bf16 output tile.
+// The MMA of block kb+1 runs while block kb is being promoted.
+//
+// Every wait is bounded (see mbar_wait): a lost arrival makes the kernel
+// record a timeout in the device error word and unwind, freeing its TMEM.
+#include "common.cuh"
+#include "launch.h"
+
+namespace fp8bw {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int NUM_THREADS = 320;
+constexpr int EPI_WARP0 = 2;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr uint32_t TMEM_COLS = 512;  // two BN-column fp32 partial buffers
+constexpr int GROUP_M = 16;          // tile raster: 16 row-blocks share a column sweep
+
+struct SharedStorage {
+  uint8_t a[STAGES][A_BYTES];  // each stage 1024-byte aligned (swizzle atom)
+  uint8_t b[STAGES][B_BYTES];
+  float sb_vec[2][2][128];     // per-row B scales: [column half][buffer][column]
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t mma_drain;          // used only when unwinding after a timeout
+  uint64_t sb_ready[2];        // per column half: its 4 warps staged this block's B scales
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+constexpr size_t kSmemBytes = sizeof(SharedStorage) + 1024;
+
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
+  const int group_size = GROUP_M * num_n;
+  const int g = tile / group_size;
+  const int first_m = g * GROUP_M;
+  const int gm = min(num_m - first_m, GROUP_M);
+  const int t = tile - g * group_size;
+  mb = first_m + t % gm;
+  nb = t / gm;
+}
+
+__device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+template <int kBScale>
+__global__ void __maxnreg__(200)
+    blockwise_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+                          const float* __restrict__ sa, int64_t sa_ld, const float* __restrict__ sb, int64_t sb_ld_nb,
+                          int64_t sb_ld_kb, uint16_t* __restrict__ out, int Mo, int No, int Kc, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  SharedStorage& sm =
+      *reinterpret_cast<SharedStorage*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_m = Mo / BM, num_n = No / BN, num_k = Kc / BK;
+  const int num_tiles = num_m * num_n;
+  const AbortFlag ab{&sm.abort_flag};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.tmem_full[b], 1);
+      mbar_init(&sm.tmem_empty[b], NUM_EPI_WARPS);
+    }
+    mbar_init(&sm.mma_drain, 1);
+    mbar_init(&sm.sb_ready[0], 4);
+    mbar_init(&sm.sb_ready[1], 4);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma_a);
+    tma_prefetch_desc(&tma_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp < EPI_WARP0) {
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;  // loads issued so far
+      bool alive = true;
+      for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, num_m, num_n, mb, nb);
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(&sm.empty[stage], phase ^ 1u, ab, status)) {
+            alive = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.full[stage], A_BYTES + B_BYTES);
+          tma_load_2d(sm.a[stage], &tma_a, &sm.full[stage], kb * BK, mb * BM);
+          tma_load_2d(sm.b[stage], &tma_b, &sm.full[stage], kb * BK, nb * BN);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!alive) {
+        // Unwinding: only the last STAGES loads can still be in flight (each
+        // earlier one was consumed before its stage was refilled).  Let them
+        // land before the CTA's shared memory is released.
+        uint32_t n = issued < STAGES ? issued : STAGES;
+        int s = stage;
+        uint32_t p = phase;
+        for (uint32_t i = 0; i < n; ++i) {
+          if (--s < 0) {
+            s = STAGES - 1;
+            p ^= 1u;
+          }
+          int dummy = 0;
+          mbar_wait(&sm.full[s], p, AbortFlag{&dummy}, status, 1000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+      int stage = 0, buf = 0;
+      uint32_t phase = 0, tphase = 0;
+      bool alive = true;
+      for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(&sm.tmem_empty[buf], tphase ^ 1u, ab, status) ||
+              !mbar_wait(&sm.full[stage], phase, ab, status)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sm.a[stage]);
+          const uint32_t b_addr = smem_u32(sm.b[stage]);
+          const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * BN);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k) {
+            mma_e4m3(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32), sdesc_kmajor_sw128(b_addr + k * 32), idesc,
+                     k > 0 ? 1u : 0u);
+          }
+          mma_commit(&sm.empty[stage]);
+          mma_commit(&sm.tmem_full[buf]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++buf == 2) {
+            buf = 0;
+            tphase ^= 1u;
+          }
+        }
+      }
+      if (!alive) {
+        // Unwinding: wait for the MMAs already issued before TMEM is freed.
+        mma_commit(&sm.mma_drain);
+        int dummy = 0;
+        mbar_wait(&sm.mma_drain, 0, AbortFlag{&dummy}, status, 1000000ull);
+      }
+    }
+  }
+  } else {
+    // ------------------------------------------------------------ promotion + epilogue
+    const int ew = warp - EPI_WARP0;
+    const int half = ew >> 2;                  // column half of the tile
+    const int quarter = warp & 3;              // TMEM lane quarter this warp may access
+    const int row = quarter * 32 + lane;       // row of the tile this thread owns
+    const int tid_half = (ew & 3) * 32 + lane; // 0..127 within the column half
+    const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+    int buf = 0;
+    uint32_t tphase = 0, sphase = 0;
+    bool alive = true;
+    for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
+      int mb, nb;
+      tile_coords(tile, num_m, num_n, mb, nb);
+      const int64_t m = static_cast<int64_t>(mb) * BM + row;
+      const int64_t col0 = static_cast<int64_t>(nb) * BN + half * 128;
+      float2 acc[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
+
+      float sa_next = __ldg(sa + m);
+      float sb_next = kBScale == 0 ? __ldg(sb + (col0 / 128) * sb_ld_nb) : __ldg(sb + col0 + tid_half);
+      for (int kb = 0; kb < num_k; ++kb) {
+        const float sa_cur = sa_next;
+        const float sb_cur = sb_next;
+        if (kb + 1 < num_k) {
+          sa_next = __ldg(sa + static_cast<int64_t>(kb + 1) * sa_ld + m);
+          sb_next = kBScale == 0 ? __ldg(sb + (col0 / 128) * sb_ld_nb + static_cast<int64_t>(kb + 1) * sb_ld_kb)
+                                 : __ldg(sb + static_cast<int64_t>(kb + 1) * sb_ld_kb + col0 + tid_half);
+        }
+        if (kBScale == 1) {
+          // Stage this block's 128 B scales of the column half.  The buffer
+          // written now was last read two blocks ago, before every warp of the
+          // half arrived on the previous block's barrier.
+          sm.sb_vec[half][kb & 1][tid_half] = sb_cur;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.sb_ready[half]);
+          const bool ok = mbar_wait(&sm.sb_ready[half], sphase, ab, status);
+          sphase ^= 1u;
+          if (!ok) {
+            alive = false;
+            break;
+          }
+        }
+        if (!mbar_wait(&sm.tmem_full[buf], tphase, ab, status)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t t_base = tmem + t_lane + static_cast<uint32_t>(buf * BN + half * 128);
+        if (kBScale == 0) {
+          const float f = sa_cur * sb_cur;
+          const float2 f2 = make_float2(f, f);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t_base + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float2 p = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+              acc[c * 16 + j] = __ffma2_rn(p, f2, acc[c * 16 + j]);
+            }
+          }
+        } else {
+          const float2 fa = make_float2(sa_cur, sa_cur);
+          const float* sbv = sm.sb_vec[half][kb & 1];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t_base + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float2 s2 = *reinterpret_cast<const float2*>(sbv + c * 32 + 2 * j);
+              const float2 p = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+              acc[c * 16 + j] = __ffma2_rn(__fmul2_rn(p, s2), fa, acc[c * 16 + j]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
+        if (++buf == 2) {
+          buf = 0;
+          tphase ^= 1u;
+        }
+      }
+      if (!alive) break;
+      uint16_t* orow = out + m * No + col0;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        st_global_v4(orow + c * 8, pack_bf16x2(acc[4 * c].x, acc[4 * c].y), pack_bf16x2(acc[4 * c + 1].x, acc[4 * c + 1].y),
+                     pack_bf16x2(acc[4 * c + 2].x, acc[4 * c + 2].y), pack_bf16x2(acc[4 * c + 3].x, acc[4 * c + 3].y));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// 2D map over a row-major [rows, cols] uint8 matrix, box = box_rows x 128
+// bytes, 128-byte swizzle.
+bool encode_kmajor_u8(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, uint32_t box_rows) {
+  auto fn = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+  cuuint32_t box[2] = {128u, box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_blockwise_gemm(const BlockwiseGemmArgs& g, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!encode_kmajor_u8(&ta, g.a, g.Mo, g.Kc, BM) || !encode_kmajor_u8(&tb, g.b, g.No, g.Kc, BN))
+    return cudaErrorInvalidValue;
+  const int num_tiles = static_cast<int>((g.Mo / BM) * (g.No / BN));
+  const int grid = num_tiles < g.num_sms ? num_tiles : g.num_sms;
+  cudaError_t e;
+  if (g.b_scale == BScale::kBlock128x128) {
+    e = cudaFuncSetAttribute(blockwise_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    blockwise_gemm_kernel<0><<<grid, NUM_THREADS, kSmemBytes, st>>>(ta, tb, g.sa, g.sa_ld, g.sb, g.sb_ld_nb, g.sb_ld_kb,
+                                                                    g.out, static_cast<int>(g.Mo),
+                                                                    static_cast<int>(g.No), static_cast<int>(g.Kc),
+                                                                    g.status);
+  } else {
+    e = cudaFuncSetAttribute(blockwise_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    blockwise_gemm_kernel<1><<<grid, NUM_THREADS, kSmemBytes, st>>>(ta, tb, g.sa, g.sa_ld, g.sb, g.sb_ld_nb, g.sb_ld_kb,
+                                                                    g.out, static_cast<int>(g.Mo),
+                                                                    static_cast<int>(g.No), static_cast<int>(g.Kc),
+                                                                    g.status);
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- bounded-wait self-test
+
+namespace {
+__global__ void selftest_wait_kernel(uint64_t limit_ns, int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, AbortFlag{&flag}, status, limit_ns);  // nothing ever arrives
+}
+}  // namespace
+
+cudaError_t launch_selftest_bounded_wait(uint32_t timeout_us, int* status, cudaStream_t st) {
+  selftest_wait_kernel<<<1, 32, 0, st>>>(static_cast<uint64_t>(timeout_us) * 1000ull, status);
+  return cudaGetLastError();
+}
+
+}  // namespace fp8bw

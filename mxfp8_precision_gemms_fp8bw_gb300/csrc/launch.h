@@ -1,0 +1,62 @@
+// Internal launchers of libfp8bw: one per kernel family.  The C ABI in
+// api.cu validates every argument, then calls these; they only configure and
+// enqueue kernels and return the launch status.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp8bw {
+
+cudaError_t launch_quant_1x128_row(const uint16_t* x, int64_t R, int64_t C, uint8_t* q, float* s, cudaStream_t st);
+cudaError_t launch_quant_1x128_col(const uint16_t* x, int64_t R, int64_t C, uint8_t* qT, float* s, cudaStream_t st);
+cudaError_t launch_quant_128x128(const uint16_t* w, int64_t R, int64_t C, uint8_t* q, uint8_t* qT, float* s,
+                                 int64_t s_ld, cudaStream_t st);
+cudaError_t launch_mx_quant_row(const uint16_t* x, int64_t R, int64_t C, uint8_t* q, uint8_t* e8, int mode,
+                                cudaStream_t st);
+cudaError_t launch_mx_quant_col(const uint16_t* x, int64_t G, int64_t R, int64_t C, uint8_t* qT, uint8_t* e8,
+                                int mode, cudaStream_t st);
+
+// Which operand-B scale structure a blockwise GEMM applies (see gemm_blockwise.cu).
+enum class BScale : int {
+  kBlock128x128 = 0,   // one scale per 128x128 block of B: sb[nb * ld_nb + kb * ld_kb]
+  kPerRow = 1          // one scale per B row per contraction block: sb[kb * ld_kb + n]
+};
+
+struct BlockwiseGemmArgs {
+  const uint8_t* a;   // [Mo, Kc] e4m3, K-major
+  const uint8_t* b;   // [No, Kc] e4m3, K-major
+  const float* sa;    // sa[kb * sa_ld + m]
+  int64_t sa_ld;
+  const float* sb;
+  int64_t sb_ld_nb;   // kBlock128x128: stride between 128-row blocks of B
+  int64_t sb_ld_kb;   // stride between contraction blocks
+  BScale b_scale;
+  uint16_t* out;      // [Mo, No] bf16
+  int64_t Mo, No, Kc;
+  int* status;
+  int num_sms;
+};
+cudaError_t launch_blockwise_gemm(const BlockwiseGemmArgs& args, cudaStream_t st);
+
+struct MxGroupedGemmArgs {
+  int kind;                   // 0 fwd, 1 dgrad, 2 wgrad
+  const uint8_t* a;
+  const uint8_t* a_e8;
+  const uint8_t* b;
+  const uint8_t* b_e8;
+  const int32_t* group_end;
+  int64_t G, M, N, K;
+  uint16_t* out;
+  int* status;
+  int num_sms;
+};
+cudaError_t launch_mx_grouped_gemm(const MxGroupedGemmArgs& args, cudaStream_t st);
+
+cudaError_t launch_selftest_bounded_wait(uint32_t timeout_us, int* status, cudaStream_t st);
+
+// cuTensorMapEncodeTiled, resolved once through the runtime's driver entry
+// point query (no link-time dependency on libcuda).
+void* tensor_map_encoder();
+
+}  // namespace fp8bw

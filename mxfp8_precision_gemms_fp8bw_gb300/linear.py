@@ -1,0 +1,142 @@
+"""Float8BlockwiseLinear and the MXFP8 MoE linear as sequences of libfp8bw calls.
+
+PR #4295 ("add FSDP and TP tests for Float8BlockwiseLinear", Summary) names a
+drop-in ``nn.Linear`` replacement whose forward is one blockwise-scaled GEMM
+and whose backward is two; PR #2386 (description) gives the block shapes.
+This module only orders the library calls and allocates their outputs with
+torch; every quantization and GEMM runs in libfp8bw's kernels.
+
+Forward   : x -> 1x128 rowwise (q_x, s_x); W -> 128x128 (q_W, q_W^T, s_W);
+            y = gemm_fwd(q_x, s_x, q_W, s_W)
+Backward  : dy -> 1x128 rowwise (q_dy, s_dy) -> dx = gemm_dgrad(q_dy, s_dy, q_W^T, s_W)
+            dy, x -> 1x128 colwise along tokens -> dW = gemm_wgrad(...)
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import binding as B
+
+
+@dataclass
+class QuantizedWeight:
+    q: torch.Tensor    # e4m3 [N, K]
+    qT: torch.Tensor   # e4m3 [K, N]
+    s: torch.Tensor    # fp32 [N/128][LD(K)]
+
+
+def quantize_weight(w: torch.Tensor, stream=None) -> QuantizedWeight:
+    q, qT, s = B.alloc_quant_128x128(w, with_transpose=True)
+    B.fp8bw_quant_128x128(w, q, qT, s, stream)
+    return QuantizedWeight(q, qT, s)
+
+
+def forward(x: torch.Tensor, wq: QuantizedWeight, stream=None):
+    """y = x W^T with x quantized 1x128 rowwise.  Returns y and (q_x, s_x)."""
+    M, K = x.shape
+    N = wq.q.shape[0]
+    xq, xs = B.alloc_quant_1x128_row(x)
+    B.fp8bw_quant_1x128_row(x, xq, xs, stream)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    B.fp8bw_gemm_fwd(xq, xs, wq.q, wq.s, y, stream)
+    return y, (xq, xs)
+
+
+def backward(dy: torch.Tensor, x: torch.Tensor, wq: QuantizedWeight, stream=None):
+    """dx = dy W and dW = dy^T x.  Returns (dx, dW)."""
+    M, N = dy.shape
+    K = x.shape[1]
+    dyq, dys = B.alloc_quant_1x128_row(dy)
+    B.fp8bw_quant_1x128_row(dy, dyq, dys, stream)
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device)
+    B.fp8bw_gemm_dgrad(dyq, dys, wq.qT, wq.s, dx, stream)
+    dyqT, dysT = B.alloc_quant_1x128_col(dy)
+    B.fp8bw_quant_1x128_col(dy, dyqT, dysT, stream)
+    xqT, xsT = B.alloc_quant_1x128_col(x)
+    B.fp8bw_quant_1x128_col(x, xqT, xsT, stream)
+    dW = torch.empty((N, K), dtype=torch.bfloat16, device=dy.device)
+    B.fp8bw_gemm_wgrad(dyqT, dysT, xqT, xsT, dW, stream)
+    return dx, dW
+
+
+class _Float8BlockwiseLinearFn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, w):
+        wq = quantize_weight(w)
+        y, _ = forward(x, wq)
+        ctx.save_for_backward(x)
+        ctx.wq = wq
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        (x,) = ctx.saved_tensors
+        dx, dW = backward(dy.contiguous(), x, ctx.wq)
+        return dx, dW
+
+
+class Float8BlockwiseLinear(torch.nn.Module):
+    """nn.Linear without bias whose three GEMMs run blockwise-scaled in e4m3.
+
+    Inputs are 2D bf16 CUDA tensors [tokens, in_features]; in_features,
+    out_features and tokens must be multiples of 128, and the output column
+    count of each GEMM (out_features for forward, in_features for both
+    gradients) a multiple of 256.
+    """
+
+    def __init__(self, in_features: int, out_features: int, device=None):
+        super().__init__()
+        self.weight = torch.nn.Parameter(torch.empty((out_features, in_features), dtype=torch.bfloat16, device=device))
+        torch.nn.init.normal_(self.weight, std=0.02)
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        return _Float8BlockwiseLinearFn.apply(x, self.weight)
+
+
+# ------------------------------------------------------------------ MXFP8 MoE linear
+
+@dataclass
+class MxExpertWeights:
+    q_row: torch.Tensor    # e4m3 [G, N, K], 1x32 along K (forward)
+    e8_row: torch.Tensor   # [G*N, K/32]
+    qT_col: torch.Tensor   # e4m3 [G, K, N], 1x32 along N (dgrad, 3D colwise)
+    e8_col: torch.Tensor   # [G, K, N/32]
+
+
+def mx_quantize_experts(w: torch.Tensor, mode: int = B.MX_RCEIL, stream=None) -> MxExpertWeights:
+    G, N, K = w.shape
+    q, e8 = B.alloc_mx_row(w.view(G * N, K))
+    B.mxfp8_quant_1x32_row(w.view(G * N, K), q, e8, mode, stream)
+    qT, e8c = B.alloc_mx_3d_col(w)
+    B.mxfp8_quant_3d_col(w, qT, e8c, mode, stream)
+    return MxExpertWeights(q.view(G, N, K), e8, qT, e8c)
+
+
+def mx_moe_forward(x: torch.Tensor, wq: MxExpertWeights, group_end: torch.Tensor, mode: int = B.MX_RCEIL, stream=None):
+    M, K = x.shape
+    G, N, _ = wq.q_row.shape
+    xq, xe = B.alloc_mx_row(x)
+    B.mxfp8_quant_1x32_row(x, xq, xe, mode, stream)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    B.mxfp8_grouped_gemm(B.GROUPED_FWD, xq, xe, wq.q_row, wq.e8_row, group_end, G, M, N, K, y, stream)
+    return y
+
+
+def mx_moe_backward(dy: torch.Tensor, x: torch.Tensor, wq: MxExpertWeights, group_end: torch.Tensor,
+                    mode: int = B.MX_RCEIL, stream=None):
+    M, N = dy.shape
+    K = x.shape[1]
+    G = wq.q_row.shape[0]
+    dyq, dye = B.alloc_mx_row(dy)
+    B.mxfp8_quant_1x32_row(dy, dyq, dye, mode, stream)
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device)
+    B.mxfp8_grouped_gemm(B.GROUPED_DGRAD, dyq, dye, wq.qT_col, wq.e8_col, group_end, G, M, N, K, dx, stream)
+    dyqT, dyeT = B.alloc_mx_col(dy)
+    B.mxfp8_quant_1x32_col(dy, dyqT, dyeT, mode, stream)
+    xqT, xeT = B.alloc_mx_col(x)
+    B.mxfp8_quant_1x32_col(x, xqT, xeT, mode, stream)
+    dW = torch.empty((G, N, K), dtype=torch.bfloat16, device=dy.device)
+    B.mxfp8_grouped_gemm(B.GROUPED_WGRAD, dyqT, dyeT, xqT, xeT, group_end, G, M, N, K, dW, stream)
+    return dx, dW

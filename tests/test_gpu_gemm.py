@@ -1,0 +1,135 @@
+"""GPU parity of the three blockwise-scaled GEMMs against the float64 oracle.
+
+Bar: max over elements of |out - ref| / (||a_i|| ||b_j||) <= 2e-3 (the
+oracle's GEMM_TOL; bf16 output rounding alone contributes up to 2^-9), and
+end-to-end SQNR >= 25 dB against the product of the unquantized bf16 inputs.
+Shapes span one tile, several tiles with more tiles than SMs, the tiny
+workload, and the full-size dense workload on sampled output rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import dense_inputs, f32, gemm_max_err, lib
+from mxfp8_precision_gemms_fp8bw_gb300 import binding as B
+from mxfp8_precision_gemms_fp8bw_gb300 import inputs
+from mxfp8_precision_gemms_fp8bw_gb300 import linear as L
+
+pytestmark = pytest.mark.gpu
+
+TOL = oracle.GEMM_TOL
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lib()
+
+
+def gpu_linear(x, w, dy):
+    xd, wd, dyd = x.cuda(), w.cuda(), dy.cuda()
+    wq = L.quantize_weight(wd)
+    y, _ = L.forward(xd, wq)
+    dx, dW = L.backward(dyd, xd, wq)
+    B.fp8bw_sync_status()
+    return f32(y), f32(dx), f32(dW)
+
+
+def oracle_linear(x, w, dy):
+    xf, wf, dyf = f32(x), f32(w), f32(dy)
+    xq, xs = oracle.quant_1x128_row(xf)
+    wq, _, ws = oracle.quant_128x128(wf)
+    dyq, dys = oracle.quant_1x128_row(dyf)
+    dyqT, dysT = oracle.quant_1x128_col(dyf)
+    xqT, xsT = oracle.quant_1x128_col(xf)
+    y = oracle.gemm_fwd(xq, xs, wq, ws)
+    dx = oracle.gemm_dgrad(dyq, dys, wq, ws)
+    dW = oracle.gemm_wgrad(dyqT, dysT, xqT, xsT)
+    deq = dict(x=oracle.dequant_1x128_row(xq, xs), w=oracle.dequant_128x128(wq, ws),
+               dy=oracle.dequant_1x128_row(dyq, dys), dyT=oracle.dequant_1x128_row(dyqT, dysT),
+               xT=oracle.dequant_1x128_row(xqT, xsT))
+    return y, dx, dW, deq
+
+
+def check_linear(x, w, dy, sqnr=True):
+    y, dx, dW = gpu_linear(x, w, dy)
+    yr, dxr, dWr, d = oracle_linear(x, w, dy)
+    e_y = gemm_max_err(y, yr, d["x"], d["w"])
+    e_dx = gemm_max_err(dx, dxr, d["dy"], d["w"].T)
+    e_dW = gemm_max_err(dW, dWr, d["dyT"], d["xT"])
+    assert e_y <= TOL and e_dx <= TOL and e_dW <= TOL, (e_y, e_dx, e_dW)
+    if sqnr:
+        xf, wf, dyf = (f32(t).astype(np.float64) for t in (x, w, dy))
+        assert oracle.sqnr_db(xf @ wf.T, y) >= oracle.SQNR_MIN_DB
+        assert oracle.sqnr_db(dyf @ wf, dx) >= oracle.SQNR_MIN_DB
+        assert oracle.sqnr_db(dyf.T @ xf, dW) >= oracle.SQNR_MIN_DB
+    return e_y, e_dx, e_dW
+
+
+def test_tiny_linear_fwd_bwd():
+    t = inputs.tiny()
+    check_linear(t.x, t.w, t.dy)
+
+
+@pytest.mark.parametrize("M,N,K,seed", [(128, 256, 256, 0), (384, 512, 768, 1), (256, 768, 1280, 2),
+                                        (2048, 4096, 512, 3)])
+def test_linear_shapes(M, N, K, seed):
+    t = inputs.linear_inputs(M, K, N, seed=100 + seed)
+    check_linear(t.x, t.w, t.dy)
+
+
+def test_zero_inputs_give_exact_zero():
+    M, N, K = 256, 256, 256
+    z = torch.zeros((M, K), dtype=torch.bfloat16)
+    w = inputs.linear_inputs(M, K, N, seed=7).w
+    y, dx, dW = gpu_linear(z, w, torch.zeros((M, N), dtype=torch.bfloat16))
+    assert np.all(y == 0) and np.all(dx == 0) and np.all(dW == 0)
+
+
+def test_integer_operands_exact():
+    # Codes of -1, 0, 1 with scales 1 or 2: every partial sum is an exact
+    # integer in fp32 and every output an integer below 2^8 in magnitude, so
+    # bf16 holds it exactly -- the GEMM must reproduce the oracle bit for bit.
+    rng = np.random.default_rng(11)
+    M, N, K = 256, 512, 384
+    xq = oracle.e4m3_encode(rng.integers(-1, 2, size=(M, K)).astype(np.float32))
+    wq = oracle.e4m3_encode(rng.integers(-1, 2, size=(N, K)).astype(np.float32))
+    xs = np.exp2(rng.integers(0, 2, size=(K // 128, M))).astype(np.float32)
+    ws = np.zeros((N // 128, B.scale_ld_128x128(K)), np.float32)
+    ws[:, :K // 128] = np.exp2(rng.integers(0, 2, size=(N // 128, K // 128)))
+    ref = oracle.gemm_fwd(xq, xs, wq, ws[:, :K // 128])
+    assert np.all(np.abs(ref) < 256) and np.all(ref == np.round(ref))
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    B.fp8bw_gemm_fwd(torch.from_numpy(xq).cuda(), torch.from_numpy(xs).cuda(), torch.from_numpy(wq).cuda(),
+                     torch.from_numpy(ws).cuda(), y)
+    B.fp8bw_sync_status()
+    assert np.array_equal(f32(y).astype(np.float64), ref)
+
+
+# ---------------------------------------------------------------- full size (sampled)
+
+def test_full_size_dense_sampled():
+    t = dense_inputs()
+    M, K = t.x.shape
+    N = t.w.shape[0]
+    y, dx, dW = gpu_linear(t.x, t.w, t.dy)
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(M, 48, replace=False))
+    xf, wf, dyf = f32(t.x), f32(t.w), f32(t.dy)
+    wq, _, ws = oracle.quant_128x128(wf)
+    wdeq = oracle.dequant_128x128(wq, ws)
+    xq, xs = oracle.quant_1x128_row(np.ascontiguousarray(xf[rows]))
+    xdeq = oracle.dequant_1x128_row(xq, xs)
+    assert gemm_max_err(y[rows], xdeq @ wdeq.T, xdeq, wdeq) <= TOL
+    dyq, dys = oracle.quant_1x128_row(np.ascontiguousarray(dyf[rows]))
+    dydeq = oracle.dequant_1x128_row(dyq, dys)
+    assert gemm_max_err(dx[rows], dydeq @ wdeq, dydeq, wdeq.T) <= TOL
+    # wgrad: 128 sampled rows n and 128 sampled columns k of dW (colwise
+    # quantization is independent per column, so the oracle quantizes only those)
+    ns = np.sort(rng.choice(N, 128, replace=False))
+    ks = np.sort(rng.choice(K, 128, replace=False))
+    dyT = oracle.quant_1x128_col(np.ascontiguousarray(dyf[:, ns]))
+    xT = oracle.quant_1x128_col(np.ascontiguousarray(xf[:, ks]))
+    a = oracle.dequant_1x128_row(*dyT)
+    b = oracle.dequant_1x128_row(*xT)
+    assert gemm_max_err(dW[np.ix_(ns, ks)], a @ b.T, a, b) <= TOL

@@ -1,0 +1,182 @@
+"""GPU parity of the quantizers: bit-exact e4m3 bytes and scale bits vs the oracle.
+
+Covers several tiles with ragged edges (MX), the edge cases of
+``gpu_util.adversarial_bf16``, both MX exponent modes, and the full-size dense
+linear workload (x[16384, 5120], W[8192, 5120], dy[16384, 8192]) compared in
+row chunks.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import adversarial_bf16, bits, dense_inputs, f32, lib, transpose_adversarial, u8
+from mxfp8_precision_gemms_fp8bw_gb300 import binding as B
+from mxfp8_precision_gemms_fp8bw_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lib()
+
+
+def run_row(x):
+    xd = x.cuda()
+    q, s = B.alloc_quant_1x128_row(xd)
+    B.fp8bw_quant_1x128_row(xd, q, s)
+    B.fp8bw_sync_status()
+    return u8(q), s.cpu().numpy()
+
+
+def run_col(x):
+    xd = x.cuda()
+    qT, s = B.alloc_quant_1x128_col(xd)
+    B.fp8bw_quant_1x128_col(xd, qT, s)
+    B.fp8bw_sync_status()
+    return u8(qT), s.cpu().numpy()
+
+
+def run_128(x, with_t=True):
+    xd = x.cuda()
+    q, qT, s = B.alloc_quant_128x128(xd, with_t)
+    B.fp8bw_quant_128x128(xd, q, qT, s)
+    B.fp8bw_sync_status()
+    return u8(q), (u8(qT) if with_t else None), s.cpu().numpy()
+
+
+@pytest.mark.parametrize("R,C,seed", [(128, 128, 0), (256, 512, 1), (384, 640, 2), (1152, 896, 3)])
+def test_1x128_row_bit_exact(R, C, seed):
+    x = adversarial_bf16(R, C, seed)
+    q, s = run_row(x)
+    qo, so = oracle.quant_1x128_row(f32(x))
+    assert np.array_equal(q, qo)
+    assert np.array_equal(bits(s), bits(so))
+
+
+@pytest.mark.parametrize("R,C,seed", [(128, 128, 4), (256, 512, 5), (640, 384, 6), (1024, 1152, 7)])
+def test_1x128_col_bit_exact(R, C, seed):
+    x = transpose_adversarial(R, C, seed)
+    qT, s = run_col(x)
+    qo, so = oracle.quant_1x128_col(f32(x))
+    assert np.array_equal(qT, qo)
+    assert np.array_equal(bits(s), bits(so))
+
+
+@pytest.mark.parametrize("R,C,seed", [(128, 128, 8), (384, 640, 9), (512, 384, 10)])
+def test_128x128_bit_exact(R, C, seed):
+    x = adversarial_bf16(R, C, seed)
+    q, qT, s = run_128(x)
+    qo, qTo, so = oracle.quant_128x128(f32(x))
+    assert np.array_equal(q, qo)
+    assert np.array_equal(qT, qTo)
+    ld = B.scale_ld_128x128(C)
+    assert s.shape == (R // 128, ld)
+    assert np.array_equal(bits(s[:, :C // 128]), bits(so))
+    assert np.all(s[:, C // 128:] == 0)         # padding untouched (allocated zeroed)
+    q2, _, s2 = run_128(x, with_t=False)        # qT is optional
+    assert np.array_equal(q2, qo) and np.array_equal(bits(s2[:, :C // 128]), bits(so))
+
+
+def test_signed_zero_and_ties_on_device():
+    # amax = 448 -> s = 1: 10.5 -> 0x52, 11.5 -> 0x54, -0.0 -> 0x80, 3*2^-10 -> 0x02.
+    row = np.zeros(128, np.float32)
+    row[:5] = [448.0, 10.5, 11.5, -0.0, 3 * 2.0 ** -10]
+    x = torch.from_numpy(np.tile(row, (128, 1))).to(torch.bfloat16)
+    q, s = run_row(x)
+    assert list(q[0, :5]) == [0x7E, 0x52, 0x54, 0x80, 0x02]
+    assert np.all(s == 1.0)
+
+
+# ---------------------------------------------------------------- MXFP8
+
+@pytest.mark.parametrize("mode", [B.MX_RCEIL, B.MX_FLOOR])
+@pytest.mark.parametrize("R,C,seed", [(32, 32, 0), (96, 160, 1), (257, 544, 2), (512, 1024, 3)])
+def test_mx_row_bit_exact(mode, R, C, seed):
+    x = adversarial_bf16(R, C, seed, block=32)
+    xd = x.cuda()
+    q, e8 = B.alloc_mx_row(xd)
+    B.mxfp8_quant_1x32_row(xd, q, e8, mode)
+    B.fp8bw_sync_status()
+    qo, eo = oracle.mx_quant_1x32_row(f32(x), mode)
+    assert np.array_equal(u8(q), qo)
+    assert np.array_equal(u8(e8), eo)
+
+
+@pytest.mark.parametrize("mode", [B.MX_RCEIL, B.MX_FLOOR])
+@pytest.mark.parametrize("R,C,seed", [(32, 8, 0), (96, 136, 1), (160, 256, 2), (544, 520, 3)])
+def test_mx_col_bit_exact(mode, R, C, seed):
+    x = transpose_adversarial(R, C, seed, block=32)
+    xd = x.cuda()
+    qT, e8 = B.alloc_mx_col(xd)
+    B.mxfp8_quant_1x32_col(xd, qT, e8, mode)
+    B.fp8bw_sync_status()
+    qo, eo = oracle.mx_quant_1x32_col(f32(x), mode)
+    assert np.array_equal(u8(qT), qo)
+    assert np.array_equal(u8(e8), eo)
+
+
+@pytest.mark.parametrize("mode", [B.MX_RCEIL, B.MX_FLOOR])
+def test_mx_3d_col_bit_exact(mode):
+    G, N, K = 3, 160, 264
+    w = torch.stack([transpose_adversarial(N, K, 10 + g, block=32) for g in range(G)])
+    wd = w.cuda()
+    qT, e8 = B.alloc_mx_3d_col(wd)
+    B.mxfp8_quant_3d_col(wd, qT, e8, mode)
+    B.fp8bw_sync_status()
+    qo, eo = oracle.mx_quant_3d_col(f32(w), mode)
+    assert np.array_equal(u8(qT), qo)
+    assert np.array_equal(u8(e8), eo)
+
+
+# ---------------------------------------------------------------- full size
+
+@pytest.fixture(scope="module")
+def dense():
+    return dense_inputs()
+
+
+def _chunks(R, step):
+    for r0 in range(0, R, step):
+        yield r0, min(R, r0 + step)
+
+
+def test_full_size_dense_row_and_col_quant(dense):
+    for t in (dense.x, dense.dy):
+        td = t.cuda()
+        q, s = B.alloc_quant_1x128_row(td)
+        B.fp8bw_quant_1x128_row(td, q, s)
+        qT, sT = B.alloc_quant_1x128_col(td)
+        B.fp8bw_quant_1x128_col(td, qT, sT)
+        B.fp8bw_sync_status()
+        q, s, qT, sT = u8(q), s.cpu().numpy(), u8(qT), sT.cpu().numpy()
+        tf = f32(t)
+        for r0, r1 in _chunks(tf.shape[0], 2048):
+            qo, so = oracle.quant_1x128_row(np.ascontiguousarray(tf[r0:r1]))
+            assert np.array_equal(q[r0:r1], qo)
+            assert np.array_equal(bits(s[:, r0:r1]), bits(so))
+            qTo, sTo = oracle.quant_1x128_col(np.ascontiguousarray(tf[r0:r1]))
+            assert np.array_equal(qT[:, r0:r1], qTo)
+            assert np.array_equal(bits(sT[r0 // 128:r1 // 128]), bits(sTo))
+
+
+def test_full_size_dense_weight_quant(dense):
+    q, qT, s = run_128(dense.w)
+    wf = f32(dense.w)
+    for r0, r1 in _chunks(wf.shape[0], 2048):
+        qo, qTo, so = oracle.quant_128x128(np.ascontiguousarray(wf[r0:r1]))
+        assert np.array_equal(q[r0:r1], qo)
+        assert np.array_equal(qT[:, r0:r1], qTo)
+        assert np.array_equal(bits(s[r0 // 128:r1 // 128, :so.shape[1]]), bits(so))
+
+
+def test_selftest_bounded_wait_reports_timeout():
+    B.fp8bw_selftest_bounded_wait(20000)          # 20 ms on a barrier nobody signals
+    with pytest.raises(B.Fp8bwError) as e:
+        B.fp8bw_sync_status()
+    assert e.value.code == B.ERR_TIMEOUT
+    B.fp8bw_sync_status()                          # the word was cleared; the context is usable
+    x = adversarial_bf16(128, 128, 0)
+    q, s = run_row(x)
+    assert np.array_equal(q, oracle.quant_1x128_row(f32(x))[0])
