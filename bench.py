@@ -1,0 +1,385 @@
+"""Benchmark of the blockwise-FP8 linear training hot path on GB300.
+
+One step = one Float8BlockwiseLinear forward+backward on the dense workload
+(M=16384 tokens, K=5120, N=8192): 1x128 quantization of x, 128x128
+quantization of W, y = x W^T, 1x128 quantization of dy, dx = dy W, colwise
+1x128 quantization of dy and x, dW = dy^T x -- eight library launches.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  `value` is the step's GEMM work (3 x 2MNK flops) over
+the device time of whole steps (quantizers included), summed over ranks.
+Inputs (520 MB bf16) and the step's outputs exceed the 129 MB L2, so no flush
+is needed between steps.  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "blockwise-FP8 GEMM TFLOPS (fwd+dgrad+wgrad) & quant GB/s, % of GB300 roofline"
+M, K, N = 16384, 5120, 8192
+WORKLOAD = f"dense Float8BlockwiseLinear fwd+bwd, M={M} K={K} N={N}, x~N(0,1) W~N(0,0.02) dy~N(0,1e-3), seed 2"
+
+# Fallback peaks (used only when MEASURED_PEAKS.json is absent).
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+FP8_OVER_BF16 = 2.0  # nominal dense ratio 4.5 / 2.25 PFLOP/s
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16": p["bf16_tflops"], "bf16_sustained": p["bf16_tflops_sustained"],
+                "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16": FALLBACK_BF16_TFLOPS, "bf16_sustained": FALLBACK_BF16_TFLOPS_SUSTAINED,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fp8bw_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={CLOCK_FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if os.environ.get("FP8BW_BENCH_GLOO") is None else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float, device) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
+
+_DENSE = None
+
+
+def dense_inputs():
+    global _DENSE
+    if _DENSE is None:
+        from mxfp8_precision_gemms_fp8bw_gb300 import inputs
+        _DENSE = inputs.dense()
+    return _DENSE
+
+
+def oracle_sample(rows: int, w_rows: int):
+    """The oracle on a bounded sample of the dense workload: the first `rows`
+    tokens of x and dy and the first `w_rows` output features of W -- every
+    quantization of the step on that sample (rowwise and colwise for x and dy,
+    128x128 for W) and the three GEMMs restricted to it (dgrad and wgrad
+    contract over the sampled features / tokens only).
+    Returns (seconds, gemm flops, threads)."""
+    import oracle
+    from mxfp8_precision_gemms_fp8bw_gb300 import inputs
+
+    t = dense_inputs()
+    x = inputs.bf16_to_f32_numpy(t.x[:rows])
+    w = inputs.bf16_to_f32_numpy(t.w[:w_rows])
+    dy = inputs.bf16_to_f32_numpy(t.dy[:rows, :w_rows])
+    t0 = time.perf_counter()
+    xq, xs = oracle.quant_1x128_row(x)
+    wq, _, ws = oracle.quant_128x128(w)
+    y = oracle.gemm_fwd(xq, xs, wq, ws)
+    dyq, dys = oracle.quant_1x128_row(dy)
+    dx = oracle.gemm_dgrad(dyq, dys, wq, ws)
+    dyqT, dysT = oracle.quant_1x128_col(dy)
+    xqT, xsT = oracle.quant_1x128_col(x)
+    dW = oracle.gemm_wgrad(dyqT, dysT, xqT, xsT)
+    secs = time.perf_counter() - t0
+    assert y.shape == (rows, w_rows) and dx.shape == (rows, K) and dW.shape == (w_rows, K)
+    threads = os.cpu_count() or 1
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        if info:
+            threads = max(i.get("num_threads", 1) for i in info)
+    except ImportError:
+        pass
+    return secs, 6 * rows * w_rows * K, threads
+
+
+def sample_desc(rows, w_rows):
+    return (f"first {rows} of {M} tokens and first {w_rows} of {N} output features: all five quantizations "
+            f"and the three GEMMs on that sample (float64 numpy oracle), GEMM flops / wall time")
+
+
+REF_SAMPLE = (128, 1024)      # per step of --impl reference (about a second)
+BASELINE_SAMPLE = (256, 8192)  # cpu_baseline of the GPU arm (tens of seconds of CPU work)
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    rows, w_rows = REF_SAMPLE
+    vals = []
+    for _ in range(args.warmup):
+        oracle_sample(rows, w_rows)
+    secs_all = []
+    for _ in range(args.steps):
+        secs, flops, threads = oracle_sample(rows, w_rows)
+        secs_all.append(secs)
+        vals.append(flops / secs / 1e12)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.median(secs_all) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample_desc(rows, w_rows)},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    from mxfp8_precision_gemms_fp8bw_gb300 import binding as B
+    from mxfp8_precision_gemms_fp8bw_gb300.linear import BlockwiseLinearWorkspace
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.lib(build_if_missing=True)
+    peaks = load_peaks()
+
+    t = dense_inputs()
+    x_h, w_h, dy_h = t.x.pin_memory(), t.w.pin_memory(), t.dy.pin_memory()
+    x, w, dy = x_h.to(dev), w_h.to(dev), dy_h.to(dev)
+    ws = BlockwiseLinearWorkspace(M, N, K, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kern = ws.kernels(x, w, dy)
+    names = [n for n, _ in kern]
+    algo = ws.algorithmic()
+
+    for _ in range(args.warmup):
+        ws.step(x, w, dy)
+    B.fp8bw_sync_status()
+
+    # Timed region: K whole steps, with an event between consecutive launches.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kern) + 1)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for s in range(args.steps):
+            evs[s][0].record(stream)
+            for i, (_, fn) in enumerate(kern):
+                fn()
+                evs[s][i + 1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    B.fp8bw_sync_status()
+    total_ms = start.elapsed_time(end)
+    total_ms = max_over_ranks(world, total_ms, dev)
+    ms_step = total_ms / args.steps
+    per_kernel = {n: statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps))
+                  for i, n in enumerate(names)}
+
+    gemm_flops = 3 * 2 * M * N * K
+    value = gemm_flops * world / (ms_step * 1e-3) / 1e12
+
+    fp8_peak = peaks["bf16_sustained"] * FP8_OVER_BF16
+    kernels = {}
+    for n in names:
+        kind, amount = algo[n]
+        ms = per_kernel[n]
+        if kind == "flops":
+            ach = amount / (ms * 1e-3) / 1e12
+            kernels[n] = {"ms": round(ms, 4), "TFLOP/s": round(ach, 1), "frac": round(ach / fp8_peak, 3)}
+        else:
+            ach = amount / (ms * 1e-3) / 1e9
+            kernels[n] = {"ms": round(ms, 4), "GB/s": round(ach, 1), "frac": round(ach / peaks["hbm_gbs"], 3)}
+    gemm_ms = sum(per_kernel[n] for n in names if algo[n][0] == "flops")
+    quant_ms = sum(per_kernel[n] for n in names if algo[n][0] == "bytes")
+    quant_bytes = sum(algo[n][1] for n in names if algo[n][0] == "bytes")
+
+    dom = max((n for n in names if algo[n][0] == "flops"), key=lambda n: per_kernel[n])
+    dom_ach = algo[dom][1] / (per_kernel[dom] * 1e-3) / 1e12
+    traffic = load_traffic(dom)
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": round(dom_ach, 1), "peak": round(fp8_peak, 1),
+                "unit": "TFLOP/s", "frac": round(dom_ach / fp8_peak, 4), "traffic": traffic,
+                "peak_source": f"{peaks['source']} sustained bf16 x {FP8_OVER_BF16:g} (nominal fp8/bf16 ratio)"}
+
+    # End to end through the public API with host buffers: H2D of the step's
+    # inputs from pinned memory, the step, D2H of its three outputs.
+    y_h = torch.empty((M, N), dtype=torch.bfloat16, pin_memory=True)
+    dx_h = torch.empty((M, K), dtype=torch.bfloat16, pin_memory=True)
+    dW_h = torch.empty((N, K), dtype=torch.bfloat16, pin_memory=True)
+    e2e_steps = max(1, min(args.steps, 10))
+    for _ in range(2):
+        _e2e_step(x, w, dy, x_h, w_h, dy_h, ws, y_h, dx_h, dW_h)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        _e2e_step(x, w, dy, x_h, w_h, dy_h, ws, y_h, dx_h, dW_h)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / e2e_steps, dev)
+    h2d = (x.numel() + w.numel() + dy.numel()) * 2
+    d2h = (y_h.numel() + dx_h.numel() + dW_h.numel()) * 2
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows, w_rows = BASELINE_SAMPLE
+        secs, flops, threads = oracle_sample(rows, w_rows)
+        cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": sample_desc(rows, w_rows), "seconds": round(secs, 2)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "parallelism": f"replicas x{world}",
+                       "l2": "inputs 520 MB and outputs exceed the 129 MB L2; no flush"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(gemm_flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": len(kern) * args.steps,
+            "clocks": clk.summary(),
+            "gemm_tflops": round(gemm_flops / (gemm_ms * 1e-3) / 1e12, 1),
+            "quant_gbs": round(quant_bytes / (quant_ms * 1e-3) / 1e9, 1),
+            "hbm_peak_gbs": peaks["hbm_gbs"],
+            "kernels": kernels,
+        }
+        print(json.dumps(line))
+    return 0
+
+
+def _e2e_step(x, w, dy, x_h, w_h, dy_h, ws, y_h, dx_h, dW_h):
+    x.copy_(x_h, non_blocking=True)
+    w.copy_(w_h, non_blocking=True)
+    dy.copy_(dy_h, non_blocking=True)
+    y, dx, dW = ws.step(x, w, dy)
+    y_h.copy_(y, non_blocking=True)
+    dx_h.copy_(dx, non_blocking=True)
+    dW_h.copy_(dW, non_blocking=True)
+
+
+def load_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            data = json.load(f)
+        from mxfp8_precision_gemms_fp8bw_gb300 import build as _b
+        if data.get("source_stamp") != _b._stamp():
+            return None
+        return data.get("kernels", {}).get(kernel)
+    except (OSError, ValueError):
+        return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

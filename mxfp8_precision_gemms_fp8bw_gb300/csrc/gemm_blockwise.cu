@@ -11,15 +11,17 @@
 // tensor core into tensor memory (TMEM) and "promoted" by CUDA cores into
 // fp32 register accumulators: acc += P_kb * sa * sb.
 //
-// Kernel structure (one persistent CTA per SM, 320 threads):
+// Kernel structure (one persistent CTA per SM, 384 threads):
 //   warp 0      TMA producer: A tile 128x128 and B tile 256x128 (e4m3,
 //               128-byte swizzle) per contraction block into a 4-stage ring.
 //   warp 1      allocates / frees the 512 TMEM columns; one thread issues 4
 //               tcgen05.mma (K = 32 each) per block into one of two 128x256
 //               fp32 TMEM partial buffers, then commits to the smem ring's
 //               "empty" barrier and to the buffer's "full" barrier.
-//   warps 2-9   promotion + epilogue: warp w reads TMEM lanes 32*(w%4)...,
-//               warps 2-5 columns 0-127 and warps 6-9 columns 128-255 of the
+//   warps 2-3   idle (they complete warpgroup 0, which gives its registers
+//               to the promotion warpgroups).
+//   warps 4-11  promotion + epilogue: warp w reads TMEM lanes 32*(w%4)...,
+//               warps 4-7 columns 0-127 and warps 8-11 columns 128-255 of the
 //               partial, multiply-add it into 128 fp32 accumulators per
 //               thread, release the buffer, and after the last block write
 //               their row of the bf16 output tile.
@@ -39,11 +41,18 @@ constexpr int BK = 128;
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
-constexpr int NUM_THREADS = 320;
-constexpr int EPI_WARP0 = 2;
+constexpr int NUM_THREADS = 384;
+constexpr int EPI_WARP0 = 4;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;  // two BN-column fp32 partial buffers
 constexpr int GROUP_M = 16;          // tile raster: 16 row-blocks share a column sweep
+// Register split.  Each SM sub-partition holds one warp of every warpgroup and
+// 16384 registers, so a 384-thread CTA launches with 168 per thread; warpgroup
+// 0 (producer, MMA, TMEM owner) then gives up registers to warpgroups 1-2
+// (promotion): 88 + 2 * 208 = 3 * 168.
+constexpr uint32_t REGS_CTRL = 88;
+constexpr uint32_t REGS_EPI = 208;
+static_assert(REGS_CTRL + 2 * REGS_EPI <= 3 * 168, "register split exceeds the launch budget");
 
 struct SharedStorage {
   uint8_t a[STAGES][A_BYTES];  // each stage 1024-byte aligned (swizzle atom)
@@ -76,7 +85,7 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, ui
 }
 
 template <int kBScale>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
     blockwise_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                           const float* __restrict__ sa, int64_t sa_ld, const float* __restrict__ sb, int64_t sb_ld_nb,
                           int64_t sb_ld_kb, uint16_t* __restrict__ out, int Mo, int No, int Kc, int* status) {
@@ -117,6 +126,7 @@ __global__ void __maxnreg__(200)
   const uint32_t tmem = sm.tmem_base;
 
   if (warp < EPI_WARP0) {
+    regs_dec<REGS_CTRL>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -203,6 +213,7 @@ __global__ void __maxnreg__(200)
     }
   }
   } else {
+    regs_inc<REGS_EPI>();
     // ------------------------------------------------------------ promotion + epilogue
     const int ew = warp - EPI_WARP0;
     const int half = ew >> 2;                  // column half of the tile
@@ -256,29 +267,29 @@ __global__ void __maxnreg__(200)
           const float f = sa_cur * sb_cur;
           const float2 f2 = make_float2(f, f);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(t_base + c * 32, r);
+          for (int c = 0; c < 8; ++c) {
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(t_base + c * 16, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < 8; ++j) {
               const float2 p = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-              acc[c * 16 + j] = __ffma2_rn(p, f2, acc[c * 16 + j]);
+              acc[c * 8 + j] = __ffma2_rn(p, f2, acc[c * 8 + j]);
             }
           }
         } else {
           const float2 fa = make_float2(sa_cur, sa_cur);
           const float* sbv = sm.sb_vec[half][kb & 1];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(t_base + c * 32, r);
+          for (int c = 0; c < 8; ++c) {
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(t_base + c * 16, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float2 s2 = *reinterpret_cast<const float2*>(sbv + c * 32 + 2 * j);
+            for (int j = 0; j < 8; ++j) {
+              const float2 s2 = *reinterpret_cast<const float2*>(sbv + c * 16 + 2 * j);
               const float2 p = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-              acc[c * 16 + j] = __ffma2_rn(__fmul2_rn(p, s2), fa, acc[c * 16 + j]);
+              acc[c * 8 + j] = __ffma2_rn(__fmul2_rn(p, s2), fa, acc[c * 8 + j]);
             }
           }
         }

@@ -140,3 +140,63 @@ def mx_moe_backward(dy: torch.Tensor, x: torch.Tensor, wq: MxExpertWeights, grou
     dW = torch.empty((G, N, K), dtype=torch.bfloat16, device=dy.device)
     B.mxfp8_grouped_gemm(B.GROUPED_WGRAD, dyqT, dyeT, xqT, xeT, group_end, G, M, N, K, dW, stream)
     return dx, dW
+
+
+# ------------------------------------------------------------------ preallocated step
+
+class BlockwiseLinearWorkspace:
+    """Every output of one Float8BlockwiseLinear forward+backward, allocated once.
+
+    ``kernels(x, w, dy)`` lists the step's library calls in order as
+    (name, callable) pairs, so a caller can time each one; ``step`` runs them.
+    Inputs: x [M, K], w [N, K], dy [M, N] bf16 on the workspace's device.
+    """
+
+    NAMES = ("quant_1x128_row(x)", "quant_128x128(W)", "gemm_fwd", "quant_1x128_row(dy)", "gemm_dgrad",
+             "quant_1x128_col(dy)", "quant_1x128_col(x)", "gemm_wgrad")
+
+    def __init__(self, M: int, N: int, K: int, device="cuda"):
+        self.M, self.N, self.K = M, N, K
+        u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)  # noqa: E731
+        self.xq, self.xs = e((M, K), u8), e((K // 128, M), f32)
+        self.wq, self.wqT = e((N, K), u8), e((K, N), u8)
+        self.ws = torch.zeros((N // 128, B.scale_ld_128x128(K)), dtype=f32, device=device)
+        self.y = e((M, N), bf)
+        self.dyq, self.dys = e((M, N), u8), e((N // 128, M), f32)
+        self.dx = e((M, K), bf)
+        self.dyqT, self.dysT = e((N, M), u8), e((M // 128, N), f32)
+        self.xqT, self.xsT = e((K, M), u8), e((M // 128, K), f32)
+        self.dW = e((N, K), bf)
+
+    def kernels(self, x, w, dy, stream=None):
+        return [
+            ("quant_1x128_row(x)", lambda: B.fp8bw_quant_1x128_row(x, self.xq, self.xs, stream)),
+            ("quant_128x128(W)", lambda: B.fp8bw_quant_128x128(w, self.wq, self.wqT, self.ws, stream)),
+            ("gemm_fwd", lambda: B.fp8bw_gemm_fwd(self.xq, self.xs, self.wq, self.ws, self.y, stream)),
+            ("quant_1x128_row(dy)", lambda: B.fp8bw_quant_1x128_row(dy, self.dyq, self.dys, stream)),
+            ("gemm_dgrad", lambda: B.fp8bw_gemm_dgrad(self.dyq, self.dys, self.wqT, self.ws, self.dx, stream)),
+            ("quant_1x128_col(dy)", lambda: B.fp8bw_quant_1x128_col(dy, self.dyqT, self.dysT, stream)),
+            ("quant_1x128_col(x)", lambda: B.fp8bw_quant_1x128_col(x, self.xqT, self.xsT, stream)),
+            ("gemm_wgrad", lambda: B.fp8bw_gemm_wgrad(self.dyqT, self.dysT, self.xqT, self.xsT, self.dW, stream)),
+        ]
+
+    def step(self, x, w, dy, stream=None):
+        for _, fn in self.kernels(x, w, dy, stream):
+            fn()
+        return self.y, self.dx, self.dW
+
+    def algorithmic(self):
+        """Per-kernel algorithmic work: bytes moved (quantizers) or flops (GEMMs)."""
+        M, N, K = self.M, self.N, self.K
+        row = lambda r, c: r * c * 3 + 4 * r * c // 128  # noqa: E731  bf16 in, e4m3 out, one fp32 per 128
+        return {
+            "quant_1x128_row(x)": ("bytes", row(M, K)),
+            "quant_128x128(W)": ("bytes", N * K * 4 + 4 * (N // 128) * (K // 128)),
+            "gemm_fwd": ("flops", 2 * M * N * K),
+            "quant_1x128_row(dy)": ("bytes", row(M, N)),
+            "gemm_dgrad": ("flops", 2 * M * N * K),
+            "quant_1x128_col(dy)": ("bytes", row(M, N)),
+            "quant_1x128_col(x)": ("bytes", row(M, K)),
+            "gemm_wgrad": ("flops", 2 * M * N * K),
+        }

@@ -114,7 +114,7 @@ def test_full_size_dense_sampled():
     N = t.w.shape[0]
     y, dx, dW = gpu_linear(t.x, t.w, t.dy)
     rng = np.random.default_rng(0)
-    rows = np.sort(rng.choice(M, 48, replace=False))
+    rows = np.sort(rng.choice(M, 128, replace=False))
     xf, wf, dyf = f32(t.x), f32(t.w), f32(t.dy)
     wq, _, ws = oracle.quant_128x128(wf)
     wdeq = oracle.dequant_128x128(wq, ws)
