@@ -49,10 +49,15 @@ constexpr int GROUP_M = 16;          // tile raster: 16 row-blocks share a colum
 // Register split.  Each SM sub-partition holds one warp of every warpgroup and
 // 16384 registers, so a 384-thread CTA launches with 168 per thread; warpgroup
 // 0 (producer, MMA, TMEM owner) then gives up registers to warpgroups 1-2
-// (promotion): 88 + 2 * 208 = 3 * 168.
-constexpr uint32_t REGS_CTRL = 88;
-constexpr uint32_t REGS_EPI = 208;
-static_assert(REGS_CTRL + 2 * REGS_EPI <= 3 * 168, "register split exceeds the launch budget");
+// (promotion): 88 + 2 * 208 = 56 + 2 * 224 = 3 * 168.
+// The per-column-scale variant holds four more live values per column pair,
+// so it takes a larger share.
+template <int kBScale>
+struct RegSplit {
+  static constexpr uint32_t ctrl = kBScale == 0 ? 88 : 56;
+  static constexpr uint32_t epi = kBScale == 0 ? 208 : 224;
+  static_assert(ctrl + 2 * epi <= 3 * 168, "register split exceeds the launch budget");
+};
 
 struct SharedStorage {
   uint8_t a[STAGES][A_BYTES];  // each stage 1024-byte aligned (swizzle atom)
@@ -126,7 +131,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem = sm.tmem_base;
 
   if (warp < EPI_WARP0) {
-    regs_dec<REGS_CTRL>();
+    regs_dec<RegSplit<kBScale>::ctrl>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
   } else {
-    regs_inc<REGS_EPI>();
+    regs_inc<RegSplit<kBScale>::epi>();
     // ------------------------------------------------------------ promotion + epilogue
     const int ew = warp - EPI_WARP0;
     const int half = ew >> 2;                  // column half of the tile
@@ -263,39 +268,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t t_base = tmem + t_lane + static_cast<uint32_t>(buf * BN + half * 128);
-        if (kBScale == 0) {
-          const float f = sa_cur * sb_cur;
-          const float2 f2 = make_float2(f, f);
+        // Two groups of four 16-column TMEM loads per block: four loads in
+        // flight per wait.  The buffer is handed back to the MMA warp as soon
+        // as the last group has landed in registers.
+        const float2 fa = make_float2(sa_cur, sa_cur);
+        const float2 f2 = kBScale == 0 ? make_float2(sa_cur * sb_cur, sa_cur * sb_cur) : fa;
+        const float* sbv = sm.sb_vec[half][kb & 1];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t r[16];
-            tmem_ld_32x32b_x16(t_base + c * 16, r);
-            tmem_ld_wait();
+        for (int g = 0; g < 2; ++g) {
+          uint32_t r[4][16];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float2 p = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-              acc[c * 8 + j] = __ffma2_rn(p, f2, acc[c * 8 + j]);
-            }
+          for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x16(t_base + (g * 4 + c) * 16, r[c]);
+          tmem_ld_wait();
+          if (g == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
           }
-        } else {
-          const float2 fa = make_float2(sa_cur, sa_cur);
-          const float* sbv = sm.sb_vec[half][kb & 1];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t r[16];
-            tmem_ld_32x32b_x16(t_base + c * 16, r);
-            tmem_ld_wait();
+          for (int c = 0; c < 4; ++c) {
+            const int col = (g * 4 + c) * 16;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float2 s2 = *reinterpret_cast<const float2*>(sbv + c * 16 + 2 * j);
-              const float2 p = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-              acc[c * 8 + j] = __ffma2_rn(__fmul2_rn(p, s2), fa, acc[c * 8 + j]);
+            for (int j = 0; j < 8; j += 2) {
+              const float2 p0 = make_float2(__uint_as_float(r[c][2 * j]), __uint_as_float(r[c][2 * j + 1]));
+              const float2 p1 = make_float2(__uint_as_float(r[c][2 * j + 2]), __uint_as_float(r[c][2 * j + 3]));
+              float2& a0 = acc[(col >> 1) + j];
+              float2& a1 = acc[(col >> 1) + j + 1];
+              if (kBScale == 0) {
+                a0 = __ffma2_rn(p0, f2, a0);
+                a1 = __ffma2_rn(p1, f2, a1);
+              } else {
+                const float4 s4 = *reinterpret_cast<const float4*>(sbv + col + 2 * j);
+                a0 = __ffma2_rn(__fmul2_rn(p0, make_float2(s4.x, s4.y)), fa, a0);
+                a1 = __ffma2_rn(__fmul2_rn(p1, make_float2(s4.z, s4.w)), fa, a1);
+              }
             }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
         if (++buf == 2) {
           buf = 0;
           tphase ^= 1u;

@@ -9,16 +9,11 @@
 // 8-byte vector.
 #include "common.cuh"
 #include "launch.h"
+#include "quant_math.cuh"
 
 namespace fp8bw {
 
 // ---------------------------------------------------------------- scale rules
-
-// Blockwise rule: s = fl32(max(amax, 1e-12) / 448), IEEE division (the EPS
-// floor of PR #4295's scale helpers; 448 = largest finite e4m3).
-__device__ __forceinline__ float blockwise_scale(float amax) {
-  return __fdiv_rn(fmaxf(amax, 1e-12f), 448.0f);
-}
 
 // MXFP8 rule: unbiased E8M0 exponent of a block from its amax.
 //   RCEIL: smallest E with 448 * 2^E >= amax.  With amax = 1.m * 2^e and
@@ -58,13 +53,13 @@ __device__ __forceinline__ float elem8(const uint4& v, int j) {
   return (j & 1) ? bf16hi_to_f32(w) : bf16lo_to_f32(w);
 }
 
-// Eight e4m3 codes of x/s (blockwise: true division) packed little-endian.
-__device__ __forceinline__ uint2 quant8_div(const uint4& v, float s) {
+// Eight e4m3 codes of fl32(x/s) packed little-endian; y = RN(1/s).
+__device__ __forceinline__ uint2 quant8_div(const uint4& v, float s, float y) {
   uint2 o;
-  o.x = cvt_e4m3x2(__fdiv_rn(bf16lo_to_f32(v.x), s), __fdiv_rn(bf16hi_to_f32(v.x), s)) |
-        (cvt_e4m3x2(__fdiv_rn(bf16lo_to_f32(v.y), s), __fdiv_rn(bf16hi_to_f32(v.y), s)) << 16);
-  o.y = cvt_e4m3x2(__fdiv_rn(bf16lo_to_f32(v.z), s), __fdiv_rn(bf16hi_to_f32(v.z), s)) |
-        (cvt_e4m3x2(__fdiv_rn(bf16lo_to_f32(v.w), s), __fdiv_rn(bf16hi_to_f32(v.w), s)) << 16);
+  o.x = cvt_e4m3x2(div_by_scale(bf16lo_to_f32(v.x), s, y), div_by_scale(bf16hi_to_f32(v.x), s, y)) |
+        (cvt_e4m3x2(div_by_scale(bf16lo_to_f32(v.y), s, y), div_by_scale(bf16hi_to_f32(v.y), s, y)) << 16);
+  o.y = cvt_e4m3x2(div_by_scale(bf16lo_to_f32(v.z), s, y), div_by_scale(bf16hi_to_f32(v.z), s, y)) |
+        (cvt_e4m3x2(div_by_scale(bf16lo_to_f32(v.w), s, y), div_by_scale(bf16hi_to_f32(v.w), s, y)) << 16);
   return o;
 }
 
@@ -119,7 +114,7 @@ __global__ void __launch_bounds__(256) quant_1x128_row_kernel(const uint16_t* __
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
     const float sc = blockwise_scale(a);
     const int rl = warp * 16 + i * 2 + half;
-    st_v2(q + (r0 + rl) * C + col, quant8_div(v[i], sc));
+    st_v2(q + (r0 + rl) * C + col, quant8_div(v[i], sc, __frcp_rn(sc)));
     if (l16 == 0) s_tile[rl] = sc;
   }
   __syncthreads();
@@ -179,8 +174,9 @@ __device__ __forceinline__ void colwise_tile(const uint16_t* __restrict__ x, int
       if ((rg & 3) == 0) e8[(col + j) * (R / 32) + row / 32] = static_cast<uint8_t>(E + 127);
     } else {
       const float sc = blockwise_scale(amax[j]);
+      const float y = __frcp_rn(sc);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) qv[i] = __fdiv_rn(elem8(v[i], j), sc);
+      for (int i = 0; i < 8; ++i) qv[i] = div_by_scale(elem8(v[i], j), sc, y);
       if (rg == j) s[(r0 / 128) * C + col + j] = sc;
     }
     uint2 o;
@@ -232,16 +228,17 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const uint16_t* __re
 #pragma unroll
   for (int w = 1; w < 8; ++w) a = fmaxf(a, warp_max[w]);
   const float sc = blockwise_scale(a);
+  const float y = __frcp_rn(sc);
   if (threadIdx.x == 0) s[blockIdx.y * s_ld + blockIdx.x] = sc;
 
 #pragma unroll
-  for (int i = 0; i < 8; ++i) st_v2(q + (row + i) * C + col, quant8_div(v[i], sc));
+  for (int i = 0; i < 8; ++i) st_v2(q + (row + i) * C + col, quant8_div(v[i], sc, y));
   if (qT != nullptr) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       float qv[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) qv[i] = __fdiv_rn(elem8(v[i], j), sc);
+      for (int i = 0; i < 8; ++i) qv[i] = div_by_scale(elem8(v[i], j), sc, y);
       uint2 o;
       o.x = cvt_e4m3x2(qv[0], qv[1]) | (cvt_e4m3x2(qv[2], qv[3]) << 16);
       o.y = cvt_e4m3x2(qv[4], qv[5]) | (cvt_e4m3x2(qv[6], qv[7]) << 16);
