@@ -22,5 +22,7 @@ def test_division_exhaustive(tmp_path):
     m = re.search(r"checked (\d+) code_mismatches (\d+)", r.stdout)
     assert m, r.stdout + r.stderr
     checked, bad = int(m.group(1)), int(m.group(2))
-    assert checked > 2_000_000_000
+    # amax over the 32640 non-negative finite bf16 patterns; for each, the
+    # 2 * (pattern + 1) bf16 values x with |x| <= amax
+    assert checked == 32640 * 32641, r.stdout
     assert bad == 0, r.stdout
