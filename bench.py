@@ -17,6 +17,8 @@ from __future__ import annotations
 
 import argparse
 import json
+
+import numpy as np
 import os
 import statistics
 import subprocess
@@ -244,41 +246,19 @@ def run_ours(args, world, rank, local):
     B.fp8bw_sync_status()
 
     # Timed region: K whole steps, with an event between consecutive launches.
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kern) + 1)] for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
-        start.record(stream)
-        for s in range(args.steps):
-            evs[s][0].record(stream)
-            for i, (_, fn) in enumerate(kern):
-                fn()
-                evs[s][i + 1].record(stream)
-        end.record(stream)
-        torch.cuda.synchronize(dev)
+        ms_step, per_kernel = time_kernels(kern, args.steps, stream)
     barrier(world)
     B.fp8bw_sync_status()
-    total_ms = start.elapsed_time(end)
-    total_ms = max_over_ranks(world, total_ms, dev)
-    ms_step = total_ms / args.steps
-    per_kernel = {n: statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps))
-                  for i, n in enumerate(names)}
+    ms_step = max_over_ranks(world, ms_step, dev)
 
     gemm_flops = 3 * 2 * M * N * K
     value = gemm_flops * world / (ms_step * 1e-3) / 1e12
 
     fp8_peak = peaks["bf16_sustained"] * FP8_OVER_BF16
-    kernels = {}
-    for n in names:
-        kind, amount = algo[n]
-        ms = per_kernel[n]
-        if kind == "flops":
-            ach = amount / (ms * 1e-3) / 1e12
-            kernels[n] = {"ms": round(ms, 4), "TFLOP/s": round(ach, 1), "frac": round(ach / fp8_peak, 3)}
-        else:
-            ach = amount / (ms * 1e-3) / 1e9
-            kernels[n] = {"ms": round(ms, 4), "GB/s": round(ach, 1), "frac": round(ach / peaks["hbm_gbs"], 3)}
+    kernels = kernel_table(per_kernel, algo, fp8_peak, peaks["hbm_gbs"])
     gemm_ms = sum(per_kernel[n] for n in names if algo[n][0] == "flops")
     quant_ms = sum(per_kernel[n] for n in names if algo[n][0] == "bytes")
     quant_bytes = sum(algo[n][1] for n in names if algo[n][0] == "bytes")
@@ -310,6 +290,9 @@ def run_ours(args, world, rank, local):
     h2d = (x.numel() + w.numel() + dy.numel()) * 2
     d2h = (y_h.numel() + dx_h.numel() + dW_h.numel()) * 2
 
+    moe = None if args.no_moe else run_moe(dev, max(10, args.steps // 3), args.warmup, fp8_peak, peaks["hbm_gbs"],
+                                           world)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rows, w_rows = BASELINE_SAMPLE
@@ -334,9 +317,83 @@ def run_ours(args, world, rank, local):
             "quant_gbs": round(quant_bytes / (quant_ms * 1e-3) / 1e9, 1),
             "hbm_peak_gbs": peaks["hbm_gbs"],
             "kernels": kernels,
+            "mxfp8_moe": moe,
         }
         print(json.dumps(line))
     return 0
+
+
+def time_kernels(kern, steps, stream):
+    """Times `steps` passes over the (name, fn) list with an event between
+    consecutive launches; returns (ms per pass, {name: mean ms})."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kern) + 1)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for s in range(steps):
+        evs[s][0].record(stream)
+        for i, (_, fn) in enumerate(kern):
+            fn()
+            evs[s][i + 1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    per = {n: statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps))
+           for i, (n, _) in enumerate(kern)}
+    return start.elapsed_time(end) / steps, per
+
+
+def kernel_table(per, algo, fp8_peak, hbm_peak):
+    out = {}
+    for n, ms in per.items():
+        kind, amount = algo[n]
+        if kind == "flops":
+            ach = amount / (ms * 1e-3) / 1e12
+            out[n] = {"ms": round(ms, 4), "TFLOP/s": round(ach, 1), "frac": round(ach / fp8_peak, 3)}
+        else:
+            ach = amount / (ms * 1e-3) / 1e9
+            out[n] = {"ms": round(ms, 4), "GB/s": round(ach, 1), "frac": round(ach / hbm_peak, 3)}
+    return out
+
+
+def run_moe(dev, steps, warmup, fp8_peak, hbm_peak, world):
+    """The MXFP8 MoE grouped linear step (M=16384 tokens over 8 experts,
+    K=5120, N=8192): nine launches, timed like the dense step."""
+    import torch
+
+    from mxfp8_precision_gemms_fp8bw_gb300 import binding as B
+    from mxfp8_precision_gemms_fp8bw_gb300 import inputs
+    from mxfp8_precision_gemms_fp8bw_gb300.linear import MxMoEWorkspace
+
+    t = inputs.moe()
+    G, N, K = t.w.shape
+    M = t.x.shape[0]
+    x, w, dy = t.x.to(dev), t.w.to(dev), t.dy.to(dev)
+    ge = torch.from_numpy(t.group_end).to(dev)
+    ws = MxMoEWorkspace(M, N, K, G, device=dev)
+    kern = ws.kernels(x, w, dy, ge)
+    for _ in range(warmup):
+        ws.step(x, w, dy, ge)
+    B.fp8bw_sync_status()
+    barrier(world)
+    ms_step, per = time_kernels(kern, steps, torch.cuda.current_stream(dev))
+    B.fp8bw_sync_status()
+    ms_step = max_over_ranks(world, ms_step, dev)
+    algo = ws.algorithmic()
+    flops = 3 * 2 * M * N * K
+    gemm_names = [n for n in per if algo[n][0] == "flops"]
+    dom = max(gemm_names, key=lambda n: per[n])
+    dom_ach = algo[dom][1] / (per[dom] * 1e-3) / 1e12
+    sizes = [int(v) for v in np.diff(np.concatenate([[0], t.group_end]))]
+    return {
+        "workload": f"MXFP8 MoE grouped linear fwd+bwd, M={M} tokens over G={G} experts (sizes {sizes}), "
+                    f"K={K}, N={N}, 1x32 E8M0 RCEIL, seed 4",
+        "value": round(flops * world / (ms_step * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "ms_per_step": round(ms_step, 4), "steps": steps, "gpu_launches": len(kern) * steps,
+        "gemm_tflops": round(flops / (sum(per[n] for n in gemm_names) * 1e-3) / 1e12, 1),
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(dom_ach, 1), "peak": round(fp8_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(dom_ach / fp8_peak, 4), "traffic": load_traffic(dom)},
+        "kernels": kernel_table(per, algo, fp8_peak, hbm_peak),
+    }
 
 
 def _e2e_step(x, w, dy, x_h, w_h, dy_h, ws, y_h, dx_h, dW_h):
@@ -373,6 +430,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-moe", action="store_true", help="skip the MXFP8 MoE section")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     world, rank, local = dist_setup(args.gpus)

@@ -268,26 +268,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t t_base = tmem + t_lane + static_cast<uint32_t>(buf * BN + half * 128);
-        // Two groups of four 16-column TMEM loads per block: four loads in
-        // flight per wait.  The buffer is handed back to the MMA warp as soon
-        // as the last group has landed in registers.
+        // 16-column TMEM loads, NC of them in flight per wait: one for the
+        // per-block B scale (eight load/wait rounds per block measured fastest),
+        // four for the per-column B scale (two rounds).  The buffer goes back
+        // to the MMA warp as soon as the last load has landed in registers.
+        constexpr int NC = kBScale == 0 ? 1 : 4;
+        constexpr int NG = 8 / NC;
         const float2 fa = make_float2(sa_cur, sa_cur);
         const float2 f2 = kBScale == 0 ? make_float2(sa_cur * sb_cur, sa_cur * sb_cur) : fa;
         const float* sbv = sm.sb_vec[half][kb & 1];
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          uint32_t r[4][16];
+        for (int g = 0; g < NG; ++g) {
+          uint32_t r[NC][16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x16(t_base + (g * 4 + c) * 16, r[c]);
+          for (int c = 0; c < NC; ++c) tmem_ld_32x32b_x16(t_base + (g * NC + c) * 16, r[c]);
           tmem_ld_wait();
-          if (g == 1) {
+          if (g == NG - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
           }
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int col = (g * 4 + c) * 16;
+          for (int c = 0; c < NC; ++c) {
+            const int col = (g * NC + c) * 16;
 #pragma unroll
             for (int j = 0; j < 8; j += 2) {
               const float2 p0 = make_float2(__uint_as_float(r[c][2 * j]), __uint_as_float(r[c][2 * j + 1]));

@@ -200,3 +200,63 @@ class BlockwiseLinearWorkspace:
             "quant_1x128_col(x)": ("bytes", row(M, K)),
             "gemm_wgrad": ("flops", 2 * M * N * K),
         }
+
+
+class MxMoEWorkspace:
+    """Every output of one MXFP8 MoE grouped linear forward+backward, allocated once.
+
+    Inputs: x [M, K], w [G, N, K], dy [M, N] bf16 and group_end int32 [G] on
+    the workspace's device.  ``kernels`` lists the step's nine library calls.
+    """
+
+    def __init__(self, M: int, N: int, K: int, G: int, device="cuda", mode: int = B.MX_RCEIL):
+        self.M, self.N, self.K, self.G, self.mode = M, N, K, G, mode
+        u8, bf = torch.uint8, torch.bfloat16
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)  # noqa: E731
+        self.xq, self.xe = e((M, K), u8), e((M, K // 32), u8)
+        self.wq, self.we = e((G * N, K), u8), e((G * N, K // 32), u8)
+        self.wqT, self.weT = e((G, K, N), u8), e((G, K, N // 32), u8)
+        self.y = e((M, N), bf)
+        self.dyq, self.dye = e((M, N), u8), e((M, N // 32), u8)
+        self.dx = e((M, K), bf)
+        self.dyqT, self.dyeT = e((N, M), u8), e((N, M // 32), u8)
+        self.xqT, self.xeT = e((K, M), u8), e((K, M // 32), u8)
+        self.dW = e((G, N, K), bf)
+
+    def kernels(self, x, w, dy, group_end, stream=None):
+        M, N, K, G, md = self.M, self.N, self.K, self.G, self.mode
+        w2 = w.view(G * N, K)
+        return [
+            ("mx_quant_1x32_row(x)", lambda: B.mxfp8_quant_1x32_row(x, self.xq, self.xe, md, stream)),
+            ("mx_quant_1x32_row(W)", lambda: B.mxfp8_quant_1x32_row(w2, self.wq, self.we, md, stream)),
+            ("mx_quant_3d_col(W)", lambda: B.mxfp8_quant_3d_col(w, self.wqT, self.weT, md, stream)),
+            ("mx_grouped_fwd", lambda: B.mxfp8_grouped_gemm(B.GROUPED_FWD, self.xq, self.xe, self.wq, self.we,
+                                                            group_end, G, M, N, K, self.y, stream)),
+            ("mx_quant_1x32_row(dy)", lambda: B.mxfp8_quant_1x32_row(dy, self.dyq, self.dye, md, stream)),
+            ("mx_grouped_dgrad", lambda: B.mxfp8_grouped_gemm(B.GROUPED_DGRAD, self.dyq, self.dye, self.wqT,
+                                                              self.weT, group_end, G, M, N, K, self.dx, stream)),
+            ("mx_quant_1x32_col(dy)", lambda: B.mxfp8_quant_1x32_col(dy, self.dyqT, self.dyeT, md, stream)),
+            ("mx_quant_1x32_col(x)", lambda: B.mxfp8_quant_1x32_col(x, self.xqT, self.xeT, md, stream)),
+            ("mx_grouped_wgrad", lambda: B.mxfp8_grouped_gemm(B.GROUPED_WGRAD, self.dyqT, self.dyeT, self.xqT,
+                                                              self.xeT, group_end, G, M, N, K, self.dW, stream)),
+        ]
+
+    def step(self, x, w, dy, group_end, stream=None):
+        for _, fn in self.kernels(x, w, dy, group_end, stream):
+            fn()
+        return self.y, self.dx, self.dW
+
+    def algorithmic(self):
+        M, N, K, G = self.M, self.N, self.K, self.G
+        mx = lambda r, c: r * c * 3 + r * c // 32  # noqa: E731  bf16 in, e4m3 out, one byte per 32
+        return {
+            "mx_quant_1x32_row(x)": ("bytes", mx(M, K)),
+            "mx_quant_1x32_row(W)": ("bytes", mx(G * N, K)),
+            "mx_quant_3d_col(W)": ("bytes", mx(G * N, K)),
+            "mx_grouped_fwd": ("flops", 2 * M * N * K),
+            "mx_quant_1x32_row(dy)": ("bytes", mx(M, N)),
+            "mx_grouped_dgrad": ("flops", 2 * M * N * K),
+            "mx_quant_1x32_col(dy)": ("bytes", mx(M, N)),
+            "mx_quant_1x32_col(x)": ("bytes", mx(M, K)),
+            "mx_grouped_wgrad": ("flops", 2 * M * N * K),
+        }
