@@ -407,19 +407,22 @@ def _e2e_step(x, w, dy, x_h, w_h, dy_h, ws, y_h, dx_h, dW_h):
 
 
 def load_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
-    was taken on the current kernel source; else None."""
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu
+    summary, if the kernel's sources still hash to what was profiled; else None."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(path):
-        return None
     try:
         with open(path) as f:
-            data = json.load(f)
-        from mxfp8_precision_gemms_fp8bw_gb300 import build as _b
-        if data.get("source_stamp") != _b._stamp():
+            entry = json.load(f)["kernels"].get(kernel)
+        if entry is None:
             return None
-        return data.get("kernels", {}).get(kernel)
-    except (OSError, ValueError):
+        from mxfp8_precision_gemms_fp8bw_gb300 import build as _b
+        h = hashlib.sha256()
+        for name in entry["sources"]:
+            with open(os.path.join(_b.CSRC, name), "rb") as f:
+                h.update(f.read())
+        return entry["bytes"] if h.hexdigest()[:16] == entry["hash"] else None
+    except (OSError, ValueError, KeyError):
         return None
 
 
