@@ -45,6 +45,7 @@
 #ifndef FP8BW_H
 #define FP8BW_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -167,8 +168,9 @@ enum fp8bw_grouped_kind { FP8BW_GROUPED_FWD = 0, FP8BW_GROUPED_DGRAD = 1, FP8BW_
  * DEVICE int32 array [G] of cumulative token counts: group g owns tokens
  * [group_end[g-1], group_end[g]) with group_end[-1] = 0; sizes must be
  * multiples of 32 (empty groups allowed) and group_end[G-1] == M.  The kernel
- * clamps every range into [0, M] and raises FP8BW_ERR_SHAPE through
- * fp8bw_sync_status when group_end breaks these rules.
+ * clamps every range into [0, M] (ends rounded down to multiples of 32) and
+ * raises FP8BW_ERR_SHAPE through fp8bw_sync_status when group_end breaks these
+ * rules.
  *   FWD   : a = xq [M, K], a_e8 [M][K/32]; b = wq [G, N, K], b_e8 [G*N][K/32]
  *           (mxfp8_quant_1x32_row of x and of w viewed as [G*N, K]);
  *           out = y bf16 [M, N]
@@ -177,12 +179,21 @@ enum fp8bw_grouped_kind { FP8BW_GROUPED_FWD = 0, FP8BW_GROUPED_DGRAD = 1, FP8BW_
  *   WGRAD : a = dyqT [N, M], a_e8 [N][M/32]; b = xqT [K, M], b_e8 [K][M/32]
  *           (mxfp8_quant_1x32_col of dy and x); out = dW bf16 [G, N, K];
  *           an empty group's dW is written as zeros.
+ * workspace: caller-owned DEVICE scratch of at least
+ * mxfp8_grouped_gemm_workspace_bytes(kind, G, M, N, K) bytes, 256-byte
+ * aligned.  The call first rewrites the scale bytes into it, in the layout the
+ * tensor core's scale-factor copy consumes, then runs the GEMM; calls that use
+ * the same workspace concurrently (on different streams) race.
  * Requirements: M multiple of 32, N and K multiples of 128, and the output
  * column count (N for FWD, K for DGRAD and WGRAD) a multiple of 256. */
 int mxfp8_grouped_gemm(int kind, const uint8_t* a, const uint8_t* a_e8,
                        const uint8_t* b, const uint8_t* b_e8, const int32_t* group_end,
                        int64_t G, int64_t M, int64_t N, int64_t K,
-                       fp8bw_bf16* out, void* stream);
+                       fp8bw_bf16* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace mxfp8_grouped_gemm needs for these dims (0 if the dims
+ * or kind are invalid).  Host-only; touches no GPU. */
+size_t mxfp8_grouped_gemm_workspace_bytes(int kind, int64_t G, int64_t M, int64_t N, int64_t K);
 
 /* ---------------------------------------------------------------------------
  * Status.

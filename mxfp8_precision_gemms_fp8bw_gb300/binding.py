@@ -36,7 +36,8 @@ _SIGNATURES = {
     "mxfp8_quant_1x32_row": [_P, _I64, _I64, _P, _P, _INT, _P],
     "mxfp8_quant_1x32_col": [_P, _I64, _I64, _P, _P, _INT, _P],
     "mxfp8_quant_3d_col": [_P, _I64, _I64, _I64, _P, _P, _INT, _P],
-    "mxfp8_grouped_gemm": [_INT, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P],
+    "mxfp8_grouped_gemm": [_INT, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, ctypes.c_size_t, _P],
+    "mxfp8_grouped_gemm_workspace_bytes": [_INT, _I64, _I64, _I64, _I64],
     "fp8bw_sync_status": [_P],
     "fp8bw_last_error": [],
     "fp8bw_selftest_bounded_wait": [ctypes.c_uint32, _P],
@@ -66,7 +67,8 @@ def lib(build_if_missing: bool = False) -> ctypes.CDLL:
         for name, args in _SIGNATURES.items():
             fn = getattr(handle, name)
             fn.argtypes = args
-            fn.restype = ctypes.c_char_p if name == "fp8bw_last_error" else ctypes.c_int
+            fn.restype = {"fp8bw_last_error": ctypes.c_char_p,
+                          "mxfp8_grouped_gemm_workspace_bytes": ctypes.c_size_t}.get(name, ctypes.c_int)
         _LIB = handle
     return _LIB
 
@@ -166,10 +168,23 @@ def fp8bw_gemm_wgrad(dyqT, dysT, xqT, xsT, dW, stream=None) -> None:
                                   _ptr(xsT, _F32, "xsT"), _ptr(dW, _BF16, "dW"), M, N, K, _stream(stream)))
 
 
-def mxfp8_grouped_gemm(kind, a, a_e8, b, b_e8, group_end, G, M, N, K, out, stream=None) -> None:
+def mxfp8_grouped_gemm_workspace_bytes(kind, G, M, N, K) -> int:
+    return int(lib().mxfp8_grouped_gemm_workspace_bytes(int(kind), G, M, N, K))
+
+
+def alloc_grouped_workspace(kind, G, M, N, K, device) -> torch.Tensor:
+    """A uint8 device buffer large enough for mxfp8_grouped_gemm's packed scales."""
+    n = mxfp8_grouped_gemm_workspace_bytes(kind, G, M, N, K)
+    if n == 0:
+        raise Fp8bwError(ERR_SHAPE, "invalid grouped GEMM dims")
+    return torch.empty(n, dtype=_U8, device=device)
+
+
+def mxfp8_grouped_gemm(kind, a, a_e8, b, b_e8, group_end, G, M, N, K, out, workspace, stream=None) -> None:
     _check(lib().mxfp8_grouped_gemm(int(kind), _ptr(a, _U8, "a"), _ptr(a_e8, _U8, "a_e8"), _ptr(b, _U8, "b"),
                                     _ptr(b_e8, _U8, "b_e8"), _ptr(group_end, _I32, "group_end"), G, M, N, K,
-                                    _ptr(out, _BF16, "out"), _stream(stream)))
+                                    _ptr(out, _BF16, "out"), _ptr(workspace, _U8, "workspace"),
+                                    workspace.numel(), _stream(stream)))
 
 
 def fp8bw_sync_status(stream=None) -> None:

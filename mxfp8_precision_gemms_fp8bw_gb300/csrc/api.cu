@@ -292,27 +292,44 @@ FP8BW_API int fp8bw_gemm_wgrad(const uint8_t* dyqT, const float* dysT, const uin
 
 // ============================================================ MXFP8 grouped GEMM
 
+static bool grouped_dims_ok(int kind, int64_t G, int64_t M, int64_t N, int64_t K) {
+  if (kind < FP8BW_GROUPED_FWD || kind > FP8BW_GROUPED_WGRAD) return false;
+  const int64_t out_cols = kind == FP8BW_GROUPED_FWD ? N : K;
+  return dim_ok(G, 1) && G <= 1024 && dim_ok(M, 32) && dim_ok(N, 128) && dim_ok(K, 128) && out_cols % 256 == 0 &&
+         G * (kind == FP8BW_GROUPED_FWD ? N : K) <= kMaxDim;
+}
+
+FP8BW_API size_t mxfp8_grouped_gemm_workspace_bytes(int kind, int64_t G, int64_t M, int64_t N, int64_t K) {
+  if (!grouped_dims_ok(kind, G, M, N, K)) return 0;
+  return fp8bw::mx_grouped_gemm_workspace_bytes(kind, G, M, N, K);
+}
+
 FP8BW_API int mxfp8_grouped_gemm(int kind, const uint8_t* a, const uint8_t* a_e8, const uint8_t* b,
                                  const uint8_t* b_e8, const int32_t* group_end, int64_t G, int64_t M, int64_t N,
-                                 int64_t K, fp8bw_bf16* out, void* stream) {
+                                 int64_t K, fp8bw_bf16* out, void* workspace, size_t workspace_bytes, void* stream) {
   const char* name = "mxfp8_grouped_gemm";
-  if (!a || !a_e8 || !b || !b_e8 || !group_end || !out)
-    return fail(FP8BW_ERR_NULL, "%s: every operand, scale, group_end and output pointer must be non-NULL", name);
+  if (!a || !a_e8 || !b || !b_e8 || !group_end || !out || !workspace)
+    return fail(FP8BW_ERR_NULL, "%s: every operand, scale, group_end, output and workspace pointer must be non-NULL",
+                name);
   if (kind < FP8BW_GROUPED_FWD || kind > FP8BW_GROUPED_WGRAD)
     return fail(FP8BW_ERR_ARG, "%s: kind %d is not FWD (0), DGRAD (1) or WGRAD (2)", name, kind);
-  const int64_t out_cols = kind == FP8BW_GROUPED_FWD ? N : K;
-  if (!dim_ok(G, 1) || G > 1024 || !dim_ok(M, 32) || !dim_ok(N, 128) || !dim_ok(K, 128) || out_cols % 256 != 0)
+  if (!grouped_dims_ok(kind, G, M, N, K))
     return fail(FP8BW_ERR_SHAPE,
                 "%s: need 0 < G <= 1024, M a multiple of 32, N and K multiples of 128 and the output column count "
-                "(%lld) a multiple of 256",
-                name, (long long)out_cols);
+                "a multiple of 256",
+                name);
   if (!aligned16(a) || !aligned16(a_e8) || !aligned16(b) || !aligned16(b_e8) || !aligned16(group_end) ||
-      !aligned16(out))
-    return fail(FP8BW_ERR_ALIGN, "%s: pointers must be 16-byte aligned", name);
+      !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(FP8BW_ERR_ALIGN, "%s: pointers must be 16-byte aligned and the workspace 256-byte aligned", name);
+  const size_t need = fp8bw::mx_grouped_gemm_workspace_bytes(kind, G, M, N, K);
+  if (workspace_bytes < need)
+    return fail(FP8BW_ERR_ARG, "%s: workspace of %zu bytes is smaller than the %zu bytes these dims need", name,
+                workspace_bytes, need);
   DeviceState* d;
   if (int rc = current_device(&d)) return rc;
   if (!fp8bw::tensor_map_encoder()) return fail(FP8BW_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", name);
-  fp8bw::MxGroupedGemmArgs g{kind, a, a_e8, b, b_e8, group_end, G, M, N, K, out, d->error_word, d->num_sms};
+  fp8bw::MxGroupedGemmArgs g{kind, a, a_e8, b, b_e8, group_end, G, M, N, K, out, workspace, workspace_bytes,
+                             d->error_word, d->num_sms};
   return launched(fp8bw::launch_mx_grouped_gemm(g, as_stream(stream)), name);
 }
 

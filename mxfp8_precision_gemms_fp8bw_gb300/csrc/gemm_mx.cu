@@ -14,20 +14,29 @@
 //   WGRAD : out[G, N, K] = dY_g^T X_g over the tokens of group g (2D x 2D)
 // FWD/DGRAD tiles are 128-token slices of one group; rows past the group's
 // end are computed with the wrong expert and never stored.  WGRAD tiles
-// contract over the group's token range in 128-wide steps, issuing only the
+// contract over the group's token range in 128-wide windows, issuing only the
 // 32-wide MMAs that lie inside the group (group sizes are multiples of 32).
 //
-// CTA (persistent, 384 threads):
-//   warp 0      TMA producer (A 128x128, B 256x128 e4m3 per stage)
-//   warp 1      TMEM owner and MMA issuer: per stage, tcgen05.cp of the
-//               stage's scale factors into TMEM, then up to 4 block-scaled
-//               MMAs (K = 32 each, scale byte j of each row's word selected
-//               by the instruction descriptor)
-//   warp 2      scale-factor gatherer: per stage, each operand row's 4 E8M0
-//               bytes into the 32-row x 16-byte interleaved layout tcgen05.cp
-//               consumes (row r -> 32-bit word (r % 32) * 4 + r / 32 of its
-//               128-row chunk)
-//   warp 3      idle
+// Scale factors reach shared memory by TMA, like the operands.  A pack kernel
+// launched just before the GEMM rewrites the row-major E8M0 bytes into
+// 512-byte chunks, one per 128 operand rows per 128-wide contraction window,
+// already in the 32-row x 16-byte interleaved layout tcgen05.cp consumes (row
+// r of the chunk -> 32-bit word (r % 32) * 4 + r / 32; byte j of the word =
+// scale of the window's j-th 32-element chunk).  The chunks live in a
+// caller-provided workspace, B's two 128-row chunks of a stage side by side:
+//   FWD/DGRAD  A: [Kc/128][M/128 + G][512 B]   (row tiles start at group starts)
+//              B: [Kc/128][G*Nout/128][512 B]
+//   WGRAD      A: [M/128 + G windows][N/128][512 B]
+//              B: [M/128 + G windows][K/128][512 B]
+// (windows: the 128-token steps of each group, numbered group after group).
+//
+// GEMM CTA (persistent, 384 threads):
+//   warp 0      TMA producer: per stage A 128x128 and B 256x128 e4m3 tiles
+//               (tensor maps) plus their 512 B + 1 KB scale chunks (bulk copies)
+//   warp 1      TMEM owner and MMA issuer: tcgen05.cp of the stage's scale
+//               chunks into TMEM, then up to 4 block-scaled MMAs (K = 32 each;
+//               the instruction descriptor selects scale byte j)
+//   warps 2-3   idle
 //   warps 4-11  epilogue: drain the accumulator (warp w: lanes 32*(w%4).., one
 //               128-column half), release it, write bf16 rows.
 #include "common.cuh"
@@ -42,24 +51,73 @@ constexpr int BK = 128;
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
+constexpr int SFA_BYTES = BM * 4;
+constexpr int SFB_BYTES = BN * 4;
 constexpr int NUM_THREADS = 384;
 constexpr int EPI_WARP0 = 4;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_COL = 0;        // accumulator: columns [0, 256)
-constexpr uint32_t SF_COL0 = 256;      // per stage: SFA 4 columns, SFB 8 columns, in 16-column slots
+constexpr uint32_t ACC_COL = 0;    // accumulator: columns [0, 256)
+constexpr uint32_t SF_COL0 = 256;  // per stage: SFA 4 columns, SFB 8 columns, in 16-column slots
 constexpr int GROUP_M = 16;
 constexpr int MAX_GROUPS = 1024;
+
+struct Problem {
+  int kind, G, M, N, K;
+  int n_out;    // output columns
+  int kc;       // FWD/DGRAD contraction length
+  int mt_max;   // FWD/DGRAD row tiles / WGRAD windows bound: M/128 + G
+  int rb_b;     // FWD/DGRAD: 128-row chunks of B (G * n_out / 128)
+  int num_nt;   // output column tiles (256 wide)
+  int num_tiles;
+};
+
+struct GroupTable {
+  int32_t start[MAX_GROUPS + 1];  // token start of each group (sanitized), start[G] = end
+  int32_t tile0[MAX_GROUPS + 1];  // first 128-token tile / window of each group; tile0[G] = total
+};
+
+// Clamps every group range into [0, M] and rounds each end down to a multiple
+// of 32 (so every token coordinate stays 32-byte aligned for TMA whatever
+// group_end holds).  Returns true when group_end broke the rules (a size that
+// is not a multiple of 32, a decreasing end, or a last end other than M).
+__device__ bool build_group_table(const int32_t* group_end, int G, int M, GroupTable& t) {
+  int prev = 0, tile0 = 0;
+  bool bad = false;
+  for (int g = 0; g < G; ++g) {
+    int e = group_end[g];
+    if (e < prev || e > M || ((e - prev) & 31) != 0) bad = true;
+    e = max(min(max(e, prev), M) & ~31, prev);
+    t.start[g] = prev;
+    t.tile0[g] = tile0;
+    tile0 += (e - prev + BM - 1) / BM;
+    prev = e;
+  }
+  if (prev != M) bad = true;
+  t.start[G] = prev;
+  t.tile0[G] = tile0;
+  return bad;
+}
+
+// The group owning 128-token tile (or window) i: the last g with tile0[g] <= i
+// (empty groups own no tile and are skipped).
+__device__ __forceinline__ int group_of(const GroupTable& t, int G, int i) {
+  int lo = 0, hi = G;  // invariant: tile0[lo] <= i < tile0[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (t.tile0[mid] <= i) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
 
 struct SharedStorage {
   uint8_t a[STAGES][A_BYTES];
   uint8_t b[STAGES][B_BYTES];
   uint32_t sfa[STAGES][BM];
   uint32_t sfb[STAGES][BN];
-  int32_t g_start[MAX_GROUPS + 1];   // token start of each group (clamped)
-  int32_t g_tile0[MAX_GROUPS + 1];   // FWD/DGRAD: first 128-row tile of each group
+  GroupTable groups;
   uint64_t full[STAGES];
-  uint64_t sf_full[STAGES];
   uint64_t empty[STAGES];
   uint64_t acc_full;
   uint64_t acc_empty;
@@ -71,23 +129,13 @@ struct SharedStorage {
 constexpr size_t kSmemBytes = sizeof(SharedStorage) + 1024;
 
 struct Tile {
-  int g;          // group
-  int a_row0;     // first row of A
-  int b_row0;     // first row of B
-  int k_begin;    // contraction range
-  int k_end;
-  int out_row0;   // first output row (FWD/DGRAD: token; WGRAD: row within dW_g)
-  int row_limit;  // output rows >= row_limit are not stored (FWD/DGRAD)
+  int g;
+  int a_row0, b_row0;           // first rows of A and B
+  int k_begin, k_end;           // contraction range
+  int out_row0, row_limit;      // first output row; rows >= row_limit are not stored
   int out_col0;
-};
-
-struct Problem {
-  int kind, G, M, N, K;
-  int n_out;      // output columns
-  int kc;         // FWD/DGRAD contraction length
-  int num_mt;     // FWD/DGRAD: 128-row tiles over all groups
-  int num_nt;     // output column tiles (256 wide)
-  int num_tiles;
+  int64_t sfa_chunk0, sfa_step;  // scale chunks of A: chunk0 + kb * step
+  int64_t sfb_chunk0, sfb_step;  // of B (two adjacent chunks per stage)
 };
 
 __device__ __forceinline__ void raster(int t, int num_m, int num_n, int& mt, int& nt) {
@@ -100,63 +148,131 @@ __device__ __forceinline__ void raster(int t, int num_m, int num_n, int& mt, int
   nt = r / gm;
 }
 
-__device__ __forceinline__ Tile decode(const SharedStorage& sm, const Problem& p, int t) {
+__device__ __forceinline__ Tile decode(const GroupTable& gt, const Problem& p, int t) {
   Tile T;
   if (p.kind != 2) {
     int mt, nt;
-    raster(t, p.num_mt, p.num_nt, mt, nt);
-    int g = 0;
-    while (g + 1 < p.G && sm.g_tile0[g + 1] <= mt) ++g;
-    const int m0 = sm.g_start[g] + (mt - sm.g_tile0[g]) * BM;
+    raster(t, gt.tile0[p.G], p.num_nt, mt, nt);
+    const int g = group_of(gt, p.G, mt);
+    const int m0 = gt.start[g] + (mt - gt.tile0[g]) * BM;
     T.g = g;
     T.a_row0 = m0;
     T.b_row0 = g * p.n_out + nt * BN;
     T.k_begin = 0;
     T.k_end = p.kc;
     T.out_row0 = m0;
-    T.row_limit = sm.g_start[g + 1];
+    T.row_limit = gt.start[g + 1];
     T.out_col0 = nt * BN;
+    T.sfa_chunk0 = mt;
+    T.sfa_step = p.mt_max;
+    T.sfb_chunk0 = T.b_row0 / BM;
+    T.sfb_step = p.rb_b;
   } else {
-    const int per_group = (p.N / BM) * p.num_nt;
+    const int rb_a = p.N / BM, rb_b = p.K / BM;
+    const int per_group = rb_a * p.num_nt;
     const int g = t / per_group;
     int mt, nt;
-    raster(t - g * per_group, p.N / BM, p.num_nt, mt, nt);
+    raster(t - g * per_group, rb_a, p.num_nt, mt, nt);
     T.g = g;
     T.a_row0 = mt * BM;
     T.b_row0 = nt * BN;
-    T.k_begin = sm.g_start[g];
-    T.k_end = sm.g_start[g + 1];
+    T.k_begin = gt.start[g];
+    T.k_end = gt.start[g + 1];
     T.out_row0 = mt * BM;
     T.row_limit = p.N;
     T.out_col0 = nt * BN;
+    T.sfa_chunk0 = static_cast<int64_t>(gt.tile0[g]) * rb_a + mt;
+    T.sfa_step = rb_a;
+    T.sfb_chunk0 = static_cast<int64_t>(gt.tile0[g]) * rb_b + T.b_row0 / BM;
+    T.sfb_step = rb_b;
   }
   return T;
 }
 
 __device__ __forceinline__ int num_kb(const Tile& T) { return (T.k_end - T.k_begin + BK - 1) / BK; }
 
-__device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) {
-  return __ldg(reinterpret_cast<const unsigned int*>(p));
+// 1D bulk copy global -> shared completing `bytes` on `bar` (16-byte aligned).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 
-// The 4 scale bytes of one operand row for contraction elements [k0, k0+128):
-// byte j = scale of chunk j; chunks at or past k_end read as 0.
-__device__ __forceinline__ uint32_t row_sf(const uint8_t* e8, int64_t row, int64_t row_bytes, int k0, int k_end,
-                                           bool aligned) {
-  const uint8_t* p = e8 + row * row_bytes + k0 / 32;
-  if (aligned && k0 + BK <= k_end) return ld_u32(p);
-  uint32_t w = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    if (k0 + 32 * j < k_end) w |= static_cast<uint32_t>(__ldg(p + j)) << (8 * j);
-  return w;
+// ---------------------------------------------------------------- scale packing
+
+// Words of the packed scale regions (see the file comment).
+__host__ __device__ inline int64_t packed_words_a(const Problem& p) {
+  return p.kind != 2 ? static_cast<int64_t>(p.kc / BK) * p.mt_max * BM
+                     : static_cast<int64_t>(p.mt_max) * (p.N / BM) * BM;
 }
+__host__ __device__ inline int64_t packed_words_b(const Problem& p) {
+  return p.kind != 2 ? static_cast<int64_t>(p.kc / BK) * p.rb_b * BM
+                     : static_cast<int64_t>(p.mt_max) * (p.K / BM) * BM;
+}
+
+// One thread per packed 32-bit word: gathers the four E8M0 bytes of one
+// operand row for one 128-wide contraction window.
+__global__ void __launch_bounds__(256) mx_pack_scales_kernel(const uint8_t* __restrict__ a_e8,
+                                                             const uint8_t* __restrict__ b_e8,
+                                                             const int32_t* __restrict__ group_end, Problem p,
+                                                             uint32_t* __restrict__ ws_a, uint32_t* __restrict__ ws_b) {
+  __shared__ GroupTable gt;
+  if (threadIdx.x == 0) build_group_table(group_end, p.G, p.M, gt);
+  __syncthreads();
+  const int64_t words_a = packed_words_a(p), total = words_a + packed_words_b(p);
+  const int64_t e8_row_bytes = (p.kind == 2 ? p.M : p.kc) / 32;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const bool is_a = i < words_a;
+    const int64_t w = is_a ? i : i - words_a;
+    const int slot = static_cast<int>(w & 127);
+    const int64_t chunk = w >> 7;
+    const int r = (slot & 3) * 32 + (slot >> 2);  // row of the 128-row chunk held by this word
+    const uint8_t* e8 = is_a ? a_e8 : b_e8;
+    uint32_t word = 0;
+    if (p.kind != 2) {
+      // chunk = kb * rows_chunks + row_chunk
+      const int rows_chunks = is_a ? p.mt_max : p.rb_b;
+      const int kb = static_cast<int>(chunk / rows_chunks);
+      const int rc = static_cast<int>(chunk - static_cast<int64_t>(kb) * rows_chunks);
+      int64_t row = -1;
+      if (is_a) {
+        if (rc < gt.tile0[p.G]) {
+          const int g = group_of(gt, p.G, rc);
+          row = gt.start[g] + static_cast<int64_t>(rc - gt.tile0[g]) * BM + r;
+          if (row >= p.M) row = -1;
+        }
+      } else {
+        row = static_cast<int64_t>(rc) * BM + r;
+      }
+      if (row >= 0) word = __ldg(reinterpret_cast<const unsigned int*>(e8 + row * e8_row_bytes + kb * 4));
+    } else {
+      // chunk = window * row_chunks + row_chunk
+      const int rows_chunks = (is_a ? p.N : p.K) / BM;
+      const int win = static_cast<int>(chunk / rows_chunks);
+      const int rc = static_cast<int>(chunk - static_cast<int64_t>(win) * rows_chunks);
+      if (win < gt.tile0[p.G]) {
+        const int g = group_of(gt, p.G, win);
+        const int k0 = gt.start[g] + (win - gt.tile0[g]) * BK;
+        const int k_end = gt.start[g + 1];
+        const uint8_t* src = e8 + (static_cast<int64_t>(rc) * BM + r) * e8_row_bytes + k0 / 32;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (k0 + 32 * j < k_end) word |= static_cast<uint32_t>(__ldg(src + j)) << (8 * j);
+      }
+    }
+    (is_a ? ws_a : ws_b)[w] = word;
+  }
+}
+
+// ---------------------------------------------------------------- GEMM
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     mx_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-                           const uint8_t* __restrict__ a_e8, const uint8_t* __restrict__ b_e8,
+                           const uint32_t* __restrict__ ws_a, const uint32_t* __restrict__ ws_b,
                            const int32_t* __restrict__ group_end, uint16_t* __restrict__ out, Problem p,
-                           int64_t a_rows, int64_t b_rows, int* status) {
+                           int* status) {
   extern __shared__ uint8_t smem_raw[];
   SharedStorage& sm =
       *reinterpret_cast<SharedStorage*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -164,30 +280,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const AbortFlag ab{&sm.abort_flag};
 
   if (threadIdx.x == 0) {
-    // Group table: clamp every range into [0, M] and round each end down to
-    // a multiple of 32 (so every TMA coordinate along tokens stays 32-byte
-    // aligned whatever group_end holds); flag sizes that are not multiples
-    // of 32, decreasing ends, or a last end other than M.
-    int prev = 0, tile0 = 0;
-    bool bad = false;
-    for (int g = 0; g < p.G; ++g) {
-      int e = group_end[g];
-      if (e < prev || e > p.M || ((e - prev) & 31) != 0) bad = true;
-      e = min(max(e, prev), p.M) & ~31;
-      e = max(e, prev);
-      sm.g_start[g] = prev;
-      sm.g_tile0[g] = tile0;
-      tile0 += (e - prev + BM - 1) / BM;
-      prev = e;
-    }
-    if (prev != p.M) bad = true;
-    sm.g_start[p.G] = prev;
-    sm.g_tile0[p.G] = tile0;
-    if (bad && blockIdx.x == 0) atomicExch(status, kStatusShape);
-    p.num_mt = tile0;
+    if (build_group_table(group_end, p.G, p.M, sm.groups) && blockIdx.x == 0) atomicExch(status, kStatusShape);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.sf_full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
     mbar_init(&sm.acc_full, 1);
@@ -195,7 +290,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(&sm.mma_drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
-    sm.g_tile0[MAX_GROUPS] = tile0;  // total 128-row tiles, read back by every thread below
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tma_a);
@@ -209,11 +303,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  if (p.kind != 2) {
-    p.num_mt = sm.g_tile0[MAX_GROUPS];
-    p.num_tiles = p.num_mt * p.num_nt;
-  }
-  const bool sf_aligned = p.kind != 2;  // FWD/DGRAD blocks start at multiples of 128
+  const GroupTable& gt = sm.groups;
+  if (p.kind != 2) p.num_tiles = gt.tile0[p.G] * p.num_nt;
 
   if (warp < EPI_WARP0) {
     regs_dec<88>();
@@ -224,7 +315,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t phase = 0, issued = 0;
         bool alive = true;
         for (int t = blockIdx.x; t < p.num_tiles && alive; t += gridDim.x) {
-          const Tile T = decode(sm, p, t);
+          const Tile T = decode(gt, p, t);
           const int nkb = num_kb(T);
           for (int kb = 0; kb < nkb; ++kb) {
             if (!mbar_wait(&sm.empty[stage], phase ^ 1u, ab, status)) {
@@ -232,9 +323,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               break;
             }
             const int k0 = T.k_begin + kb * BK;
-            mbar_arrive_expect_tx(&sm.full[stage], A_BYTES + B_BYTES);
+            mbar_arrive_expect_tx(&sm.full[stage], A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES);
             tma_load_2d(sm.a[stage], &tma_a, &sm.full[stage], k0, T.a_row0);
             tma_load_2d(sm.b[stage], &tma_b, &sm.full[stage], k0, T.b_row0);
+            bulk_load(sm.sfa[stage], ws_a + (T.sfa_chunk0 + kb * T.sfa_step) * BM, SFA_BYTES, &sm.full[stage]);
+            bulk_load(sm.sfb[stage], ws_b + (T.sfb_chunk0 + kb * T.sfb_step) * BM, SFB_BYTES, &sm.full[stage]);
             ++issued;
             if (++stage == STAGES) {
               stage = 0;
@@ -243,6 +336,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         if (!alive) {
+          // Unwinding: only the last STAGES loads can still be in flight.
           uint32_t n = issued < STAGES ? issued : STAGES;
           int s = stage;
           uint32_t ph = phase;
@@ -263,7 +357,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t phase = 0, aphase = 0;
         bool alive = true;
         for (int t = blockIdx.x; t < p.num_tiles && alive; t += gridDim.x) {
-          const Tile T = decode(sm, p, t);
+          const Tile T = decode(gt, p, t);
           const int nkb = num_kb(T);
           if (nkb == 0) continue;  // empty WGRAD group: the epilogue writes zeros
           if (!mbar_wait(&sm.acc_empty, aphase ^ 1u, ab, status)) {
@@ -272,7 +366,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           for (int kb = 0; kb < nkb; ++kb) {
-            if (!mbar_wait(&sm.full[stage], phase, ab, status) || !mbar_wait(&sm.sf_full[stage], phase, ab, status)) {
+            if (!mbar_wait(&sm.full[stage], phase, ab, status)) {
               alive = false;
               break;
             }
@@ -306,44 +400,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_wait(&sm.mma_drain, 0, AbortFlag{&dummy}, status, 1000000ull);
         }
       }
-    } else if (warp == 2) {
-      // ------------------------------------------------------------ scale-factor gatherer
-      int stage = 0;
-      uint32_t phase = 0;
-      bool alive = true;
-      const int64_t a_row_bytes = (p.kind == 2 ? p.M : p.kc) / 32;
-      for (int t = blockIdx.x; t < p.num_tiles && alive; t += gridDim.x) {
-        const Tile T = decode(sm, p, t);
-        const int nkb = num_kb(T);
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&sm.empty[stage], phase ^ 1u, ab, status)) {
-            alive = false;
-            break;
-          }
-          const int k0 = T.k_begin + kb * BK;
-#pragma unroll
-          for (int i = 0; i < BM / 32; ++i) {
-            const int r = i * 32 + lane;
-            const int64_t row = T.a_row0 + r;
-            const uint32_t w = row < a_rows ? row_sf(a_e8, row, a_row_bytes, k0, T.k_end, sf_aligned) : 0u;
-            sm.sfa[stage][(r & 31) * 4 + (r >> 5)] = w;
-          }
-#pragma unroll
-          for (int i = 0; i < BN / 32; ++i) {
-            const int r = i * 32 + lane;
-            const int64_t row = T.b_row0 + r;
-            const uint32_t w = row < b_rows ? row_sf(b_e8, row, a_row_bytes, k0, T.k_end, sf_aligned) : 0u;
-            sm.sfb[stage][(r >> 7) * 128 + (r & 31) * 4 + ((r >> 5) & 3)] = w;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.sf_full[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
     }
   } else {
     regs_inc<208>();
@@ -355,7 +411,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t aphase = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      const Tile T = decode(sm, p, t);
+      const Tile T = decode(gt, p, t);
       const int nkb = num_kb(T);
       const int out_row = T.out_row0 + row;
       const bool store = out_row < T.row_limit;
@@ -428,44 +484,63 @@ bool encode_kmajor_u8(CUtensorMap* map, const void* base, int64_t rows, int64_t 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+Problem make_problem(int kind, int64_t G, int64_t M, int64_t N, int64_t K) {
+  Problem p{};
+  p.kind = kind;
+  p.G = static_cast<int>(G);
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.n_out = kind == 0 ? p.N : p.K;
+  p.kc = kind == 0 ? p.K : (kind == 1 ? p.N : p.M);
+  p.mt_max = p.M / BM + p.G;
+  p.rb_b = kind == 2 ? 0 : p.G * p.n_out / BM;
+  p.num_nt = p.n_out / BN;
+  // FWD/DGRAD: the kernel takes the exact count from group_end; this is its bound.
+  p.num_tiles = kind == 2 ? p.G * (p.N / BM) * p.num_nt : p.mt_max * p.num_nt;
+  return p;
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
 }  // namespace
 
+size_t mx_grouped_gemm_workspace_bytes(int kind, int64_t G, int64_t M, int64_t N, int64_t K) {
+  const Problem p = make_problem(kind, G, M, N, K);
+  return align_up(static_cast<size_t>(packed_words_a(p)) * 4) + align_up(static_cast<size_t>(packed_words_b(p)) * 4);
+}
+
 cudaError_t launch_mx_grouped_gemm(const MxGroupedGemmArgs& g, cudaStream_t st) {
-  Problem p{};
-  p.kind = g.kind;
-  p.G = static_cast<int>(g.G);
-  p.M = static_cast<int>(g.M);
-  p.N = static_cast<int>(g.N);
-  p.K = static_cast<int>(g.K);
+  const Problem p = make_problem(g.kind, g.G, g.M, g.N, g.K);
   int64_t a_rows, a_cols, b_rows, b_cols;
   if (g.kind == 0) {          // FWD: A = x [M, K], B = W [G*N, K]
-    p.n_out = p.N;
-    p.kc = p.K;
     a_rows = g.M, a_cols = g.K, b_rows = g.G * g.N, b_cols = g.K;
   } else if (g.kind == 1) {   // DGRAD: A = dy [M, N], B = W^T [G*K, N]
-    p.n_out = p.K;
-    p.kc = p.N;
     a_rows = g.M, a_cols = g.N, b_rows = g.G * g.K, b_cols = g.N;
   } else {                    // WGRAD: A = dy^T [N, M], B = x^T [K, M]
-    p.n_out = p.K;
-    p.kc = p.M;
     a_rows = g.N, a_cols = g.M, b_rows = g.K, b_cols = g.M;
   }
-  p.num_nt = p.n_out / BN;
-  // FWD/DGRAD: at most M/128 + G row tiles; the kernel computes the exact
-  // count from group_end and skips the tiles past it.
-  const int max_mt = p.M / BM + p.G;
-  p.num_mt = max_mt;
-  p.num_tiles = g.kind == 2 ? p.G * (p.N / BM) * p.num_nt : max_mt * p.num_nt;
+  if (g.workspace_bytes < mx_grouped_gemm_workspace_bytes(g.kind, g.G, g.M, g.N, g.K)) return cudaErrorInvalidValue;
+  uint32_t* ws_a = static_cast<uint32_t*>(g.workspace);
+  uint32_t* ws_b = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(g.workspace) +
+                                               align_up(static_cast<size_t>(packed_words_a(p)) * 4));
   CUtensorMap ta, tb;
   if (!encode_kmajor_u8(&ta, g.a, a_rows, a_cols, BM) || !encode_kmajor_u8(&tb, g.b, b_rows, b_cols, BN))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(mx_grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
+
+  const int64_t words = packed_words_a(p) + packed_words_b(p);
+  const int64_t pack_blocks = (words + 255) / 256;
+  const int pack_grid = static_cast<int>(pack_blocks < 8LL * g.num_sms ? pack_blocks : 8LL * g.num_sms);
+  mx_pack_scales_kernel<<<pack_grid, 256, 0, st>>>(g.a_e8, g.b_e8, g.group_end, p, ws_a, ws_b);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  e = cudaFuncSetAttribute(mx_grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   const int grid = p.num_tiles < g.num_sms ? p.num_tiles : g.num_sms;
-  mx_grouped_gemm_kernel<<<grid, NUM_THREADS, kSmemBytes, st>>>(ta, tb, g.a_e8, g.b_e8, g.group_end, g.out, p, a_rows,
-                                                                b_rows, g.status);
+  mx_grouped_gemm_kernel<<<grid, NUM_THREADS, kSmemBytes, st>>>(ta, tb, ws_a, ws_b, g.group_end, g.out, p, g.status);
   return cudaGetLastError();
 }
 

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 namespace fp8bw {
@@ -48,9 +49,12 @@ struct MxGroupedGemmArgs {
   const int32_t* group_end;
   int64_t G, M, N, K;
   uint16_t* out;
+  void* workspace;            // packed scale factors (mx_grouped_gemm_workspace_bytes)
+  size_t workspace_bytes;
   int* status;
   int num_sms;
 };
+size_t mx_grouped_gemm_workspace_bytes(int kind, int64_t G, int64_t M, int64_t N, int64_t K);
 cudaError_t launch_mx_grouped_gemm(const MxGroupedGemmArgs& args, cudaStream_t st);
 
 cudaError_t launch_selftest_bounded_wait(uint32_t timeout_us, int* status, cudaStream_t st);

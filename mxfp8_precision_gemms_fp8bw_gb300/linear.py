@@ -120,7 +120,8 @@ def mx_moe_forward(x: torch.Tensor, wq: MxExpertWeights, group_end: torch.Tensor
     xq, xe = B.alloc_mx_row(x)
     B.mxfp8_quant_1x32_row(x, xq, xe, mode, stream)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    B.mxfp8_grouped_gemm(B.GROUPED_FWD, xq, xe, wq.q_row, wq.e8_row, group_end, G, M, N, K, y, stream)
+    ws = B.alloc_grouped_workspace(B.GROUPED_FWD, G, M, N, K, x.device)
+    B.mxfp8_grouped_gemm(B.GROUPED_FWD, xq, xe, wq.q_row, wq.e8_row, group_end, G, M, N, K, y, ws, stream)
     return y
 
 
@@ -132,13 +133,15 @@ def mx_moe_backward(dy: torch.Tensor, x: torch.Tensor, wq: MxExpertWeights, grou
     dyq, dye = B.alloc_mx_row(dy)
     B.mxfp8_quant_1x32_row(dy, dyq, dye, mode, stream)
     dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device)
-    B.mxfp8_grouped_gemm(B.GROUPED_DGRAD, dyq, dye, wq.qT_col, wq.e8_col, group_end, G, M, N, K, dx, stream)
+    ws = B.alloc_grouped_workspace(B.GROUPED_DGRAD, G, M, N, K, dy.device)
+    B.mxfp8_grouped_gemm(B.GROUPED_DGRAD, dyq, dye, wq.qT_col, wq.e8_col, group_end, G, M, N, K, dx, ws, stream)
     dyqT, dyeT = B.alloc_mx_col(dy)
     B.mxfp8_quant_1x32_col(dy, dyqT, dyeT, mode, stream)
     xqT, xeT = B.alloc_mx_col(x)
     B.mxfp8_quant_1x32_col(x, xqT, xeT, mode, stream)
     dW = torch.empty((G, N, K), dtype=torch.bfloat16, device=dy.device)
-    B.mxfp8_grouped_gemm(B.GROUPED_WGRAD, dyqT, dyeT, xqT, xeT, group_end, G, M, N, K, dW, stream)
+    ws = B.alloc_grouped_workspace(B.GROUPED_WGRAD, G, M, N, K, dy.device)
+    B.mxfp8_grouped_gemm(B.GROUPED_WGRAD, dyqT, dyeT, xqT, xeT, group_end, G, M, N, K, dW, ws, stream)
     return dx, dW
 
 
@@ -222,6 +225,7 @@ class MxMoEWorkspace:
         self.dyqT, self.dyeT = e((N, M), u8), e((N, M // 32), u8)
         self.xqT, self.xeT = e((K, M), u8), e((K, M // 32), u8)
         self.dW = e((G, N, K), bf)
+        self.ws = e((max(B.mxfp8_grouped_gemm_workspace_bytes(k, G, M, N, K) for k in range(3)),), u8)
 
     def kernels(self, x, w, dy, group_end, stream=None):
         M, N, K, G, md = self.M, self.N, self.K, self.G, self.mode
@@ -231,14 +235,14 @@ class MxMoEWorkspace:
             ("mx_quant_1x32_row(W)", lambda: B.mxfp8_quant_1x32_row(w2, self.wq, self.we, md, stream)),
             ("mx_quant_3d_col(W)", lambda: B.mxfp8_quant_3d_col(w, self.wqT, self.weT, md, stream)),
             ("mx_grouped_fwd", lambda: B.mxfp8_grouped_gemm(B.GROUPED_FWD, self.xq, self.xe, self.wq, self.we,
-                                                            group_end, G, M, N, K, self.y, stream)),
+                                                            group_end, G, M, N, K, self.y, self.ws, stream)),
             ("mx_quant_1x32_row(dy)", lambda: B.mxfp8_quant_1x32_row(dy, self.dyq, self.dye, md, stream)),
             ("mx_grouped_dgrad", lambda: B.mxfp8_grouped_gemm(B.GROUPED_DGRAD, self.dyq, self.dye, self.wqT,
-                                                              self.weT, group_end, G, M, N, K, self.dx, stream)),
+                                                              self.weT, group_end, G, M, N, K, self.dx, self.ws, stream)),
             ("mx_quant_1x32_col(dy)", lambda: B.mxfp8_quant_1x32_col(dy, self.dyqT, self.dyeT, md, stream)),
             ("mx_quant_1x32_col(x)", lambda: B.mxfp8_quant_1x32_col(x, self.xqT, self.xeT, md, stream)),
             ("mx_grouped_wgrad", lambda: B.mxfp8_grouped_gemm(B.GROUPED_WGRAD, self.dyqT, self.dyeT, self.xqT,
-                                                              self.xeT, group_end, G, M, N, K, self.dW, stream)),
+                                                              self.xeT, group_end, G, M, N, K, self.dW, self.ws, stream)),
         ]
 
     def step(self, x, w, dy, group_end, stream=None):

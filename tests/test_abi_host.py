@@ -30,6 +30,7 @@ def test_header_declares_the_abi():
         "fp8bw_quant_1x128_row", "fp8bw_quant_1x128_col", "fp8bw_quant_128x128",
         "fp8bw_gemm_fwd", "fp8bw_gemm_dgrad", "fp8bw_gemm_wgrad",
         "mxfp8_quant_1x32_row", "mxfp8_quant_1x32_col", "mxfp8_quant_3d_col", "mxfp8_grouped_gemm",
+        "mxfp8_grouped_gemm_workspace_bytes",
         "fp8bw_sync_status", "fp8bw_last_error", "fp8bw_selftest_bounded_wait",
     ])
 
@@ -57,7 +58,8 @@ def test_null_pointers_rejected(L):
     assert L.fp8bw_quant_1x128_row(None, 128, 128, P, P * 2, None) == binding.ERR_NULL
     assert "non-NULL" in binding.last_error()
     assert L.fp8bw_gemm_fwd(P, P, None, P, P, 128, 256, 128, None) == binding.ERR_NULL
-    assert L.mxfp8_grouped_gemm(0, P, P, P, P, None, 1, 32, 256, 128, P, None) == binding.ERR_NULL
+    assert L.mxfp8_grouped_gemm(0, P, P, P, P, None, 1, 32, 256, 128, P, 64 * P, 1 << 20, None) == binding.ERR_NULL
+    assert L.mxfp8_grouped_gemm(0, P, P, P, P, P, 1, 32, 256, 128, P, None, 1 << 20, None) == binding.ERR_NULL
 
 
 @pytest.mark.parametrize("R,C", [(0, 128), (128, 0), (100, 128), (128, 200), (-128, 128)])
@@ -86,7 +88,8 @@ def test_misaligned_pointers_rejected(L):
 def test_enum_arguments_rejected(L):
     assert L.mxfp8_quant_1x32_row(P, 32, 32, 64 * P, 128 * P, 2, None) == binding.ERR_ARG
     assert L.mxfp8_quant_3d_col(P, 2, 64, 64, 64 * P, 128 * P, -1, None) == binding.ERR_ARG
-    assert L.mxfp8_grouped_gemm(3, P, 2 * P, 3 * P, 4 * P, 5 * P, 1, 32, 256, 128, 64 * P, None) == binding.ERR_ARG
+    assert L.mxfp8_grouped_gemm(3, P, 2 * P, 3 * P, 4 * P, 5 * P, 1, 32, 256, 128, 64 * P, 128 * P, 1 << 20,
+                                None) == binding.ERR_ARG
     assert L.fp8bw_selftest_bounded_wait(0, None) == binding.ERR_ARG
     assert L.fp8bw_selftest_bounded_wait(3000000, None) == binding.ERR_ARG
 
@@ -113,3 +116,20 @@ def test_binding_rejects_wrong_dtype_and_layout():
         binding._ptr(x, torch.bfloat16, "x")
     with pytest.raises(ValueError):
         binding._ptr(torch.zeros(128, 128, dtype=torch.bfloat16), torch.bfloat16, "x")  # CPU tensor
+
+
+def test_grouped_workspace_size_is_host_only(L):
+    n = L.mxfp8_grouped_gemm_workspace_bytes(0, 8, 16384, 8192, 5120)
+    # FWD: A chunks (M/128 + G) x K/128, B chunks G*N/128 x K/128, 512 bytes each
+    assert n == (136 * 40 + 512 * 40) * 512
+    assert L.mxfp8_grouped_gemm_workspace_bytes(2, 8, 16384, 8192, 5120) == 136 * (64 + 40) * 512
+    assert L.mxfp8_grouped_gemm_workspace_bytes(5, 8, 16384, 8192, 5120) == 0
+    assert L.mxfp8_grouped_gemm_workspace_bytes(0, 8, 100, 8192, 5120) == 0
+
+
+def test_grouped_rejects_small_or_misaligned_workspace(L):
+    need = L.mxfp8_grouped_gemm_workspace_bytes(0, 2, 256, 256, 256)
+    args = (0, P, 2 * P, 3 * P, 4 * P, 5 * P, 2, 256, 256, 256, 64 * P)
+    assert L.mxfp8_grouped_gemm(*args, 128 * P, need - 1, None) == binding.ERR_ARG
+    assert "workspace" in binding.last_error()
+    assert L.mxfp8_grouped_gemm(*args, 128 * P + 16, need, None) == binding.ERR_ALIGN
