@@ -195,6 +195,32 @@ int mxfp8_grouped_gemm(int kind, const uint8_t* a, const uint8_t* a_e8,
  * or kind are invalid).  Host-only; touches no GPU. */
 size_t mxfp8_grouped_gemm_workspace_bytes(int kind, int64_t G, int64_t M, int64_t N, int64_t K);
 
+/* Largest scratch, in bytes, mxfp8_grouped_gemm_noalloc can use. */
+#define FP8BW_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* mxfp8_grouped_gemm for callers that cannot allocate device memory: code that
+ * only receives device pointers from a framework owning every allocation
+ * (its caching allocator), or a training/serving loop whose device footprint
+ * is fixed before the first step.  It computes exactly what
+ * mxfp8_grouped_gemm computes, with the same arguments minus the workspace;
+ * the scratch lives in a fixed array of FP8BW_NOALLOC_SCRATCH_BYTES (16 MiB)
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.  The pages describe nothing like it; it is an addition for
+ * such callers.
+ * - Dims whose mxfp8_grouped_gemm_workspace_bytes exceeds that size are
+ *   rejected with FP8BW_ERR_SHAPE and a message naming both sizes.
+ * - The first call on a device resolves the array's device address for that
+ *   device (with that device current); make that first call before any stream
+ *   capture.  No call allocates or frees device memory.
+ * - Every call on a device shares the one array and leaves its contents
+ *   behind; each call rewrites all of the scratch it reads, so nothing needs
+ *   to start at zero.  Calls whose executions overlap on the GPU (different
+ *   streams, same device) race on the array and give wrong results. */
+int mxfp8_grouped_gemm_noalloc(int kind, const uint8_t* a, const uint8_t* a_e8,
+                               const uint8_t* b, const uint8_t* b_e8, const int32_t* group_end,
+                               int64_t G, int64_t M, int64_t N, int64_t K,
+                               fp8bw_bf16* out, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Status.
  * ------------------------------------------------------------------------- */

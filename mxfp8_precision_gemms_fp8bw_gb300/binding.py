@@ -38,6 +38,7 @@ _SIGNATURES = {
     "mxfp8_quant_3d_col": [_P, _I64, _I64, _I64, _P, _P, _INT, _P],
     "mxfp8_grouped_gemm": [_INT, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, ctypes.c_size_t, _P],
     "mxfp8_grouped_gemm_workspace_bytes": [_INT, _I64, _I64, _I64, _I64],
+    "mxfp8_grouped_gemm_noalloc": [_INT, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P],
     "fp8bw_sync_status": [_P],
     "fp8bw_last_error": [],
     "fp8bw_selftest_bounded_wait": [ctypes.c_uint32, _P],
@@ -185,6 +186,17 @@ def mxfp8_grouped_gemm(kind, a, a_e8, b, b_e8, group_end, G, M, N, K, out, works
                                     _ptr(b_e8, _U8, "b_e8"), _ptr(group_end, _I32, "group_end"), G, M, N, K,
                                     _ptr(out, _BF16, "out"), _ptr(workspace, _U8, "workspace"),
                                     workspace.numel(), _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def mxfp8_grouped_gemm_noalloc(kind, a, a_e8, b, b_e8, group_end, G, M, N, K, out, stream=None) -> None:
+    """mxfp8_grouped_gemm without a workspace argument: for callers that cannot
+    allocate device memory, the library uses its own fixed 16 MiB array."""
+    _check(lib().mxfp8_grouped_gemm_noalloc(int(kind), _ptr(a, _U8, "a"), _ptr(a_e8, _U8, "a_e8"), _ptr(b, _U8, "b"),
+                                            _ptr(b_e8, _U8, "b_e8"), _ptr(group_end, _I32, "group_end"), G, M, N, K,
+                                            _ptr(out, _BF16, "out"), _stream(stream)))
 
 
 def fp8bw_sync_status(stream=None) -> None:

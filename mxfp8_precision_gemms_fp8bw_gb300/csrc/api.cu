@@ -333,6 +333,40 @@ FP8BW_API int mxfp8_grouped_gemm(int kind, const uint8_t* a, const uint8_t* a_e8
   return launched(fp8bw::launch_mx_grouped_gemm(g, as_stream(stream)), name);
 }
 
+// Same checks and launch as mxfp8_grouped_gemm, with the library's fixed
+// scratch array in place of a caller workspace; nothing is allocated.
+FP8BW_API int mxfp8_grouped_gemm_noalloc(int kind, const uint8_t* a, const uint8_t* a_e8, const uint8_t* b,
+                                         const uint8_t* b_e8, const int32_t* group_end, int64_t G, int64_t M,
+                                         int64_t N, int64_t K, fp8bw_bf16* out, void* stream) {
+  const char* name = "mxfp8_grouped_gemm_noalloc";
+  if (!a || !a_e8 || !b || !b_e8 || !group_end || !out)
+    return fail(FP8BW_ERR_NULL, "%s: every operand, scale, group_end and output pointer must be non-NULL", name);
+  if (kind < FP8BW_GROUPED_FWD || kind > FP8BW_GROUPED_WGRAD)
+    return fail(FP8BW_ERR_ARG, "%s: kind %d is not FWD (0), DGRAD (1) or WGRAD (2)", name, kind);
+  if (!grouped_dims_ok(kind, G, M, N, K))
+    return fail(FP8BW_ERR_SHAPE,
+                "%s: need 0 < G <= 1024, M a multiple of 32, N and K multiples of 128 and the output column count "
+                "a multiple of 256",
+                name);
+  const size_t need = fp8bw::mx_grouped_gemm_workspace_bytes(kind, G, M, N, K);
+  if (need > fp8bw::kStaticScratchBytes)
+    return fail(FP8BW_ERR_SHAPE, "%s: these dims need %zu bytes of scratch, more than the fixed %zu-byte array",
+                name, need, fp8bw::kStaticScratchBytes);
+  if (!aligned16(a) || !aligned16(a_e8) || !aligned16(b) || !aligned16(b_e8) || !aligned16(group_end) ||
+      !aligned16(out))
+    return fail(FP8BW_ERR_ALIGN, "%s: pointers must be 16-byte aligned", name);
+  DeviceState* d;
+  if (int rc = current_device(&d)) return rc;
+  if (!fp8bw::tensor_map_encoder()) return fail(FP8BW_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", name);
+  void* scratch = nullptr;
+  cudaError_t e = fp8bw::static_scratch_address(&scratch);
+  if (e != cudaSuccess)
+    return fail(FP8BW_ERR_CUDA, "%s: resolving the scratch array's device address: %s", name, cudaGetErrorString(e));
+  fp8bw::MxGroupedGemmArgs g{kind, a, a_e8, b, b_e8, group_end, G, M, N, K, out, scratch,
+                             fp8bw::kStaticScratchBytes, d->error_word, d->num_sms};
+  return launched(fp8bw::launch_mx_grouped_gemm(g, as_stream(stream)), name);
+}
+
 // ============================================================ status
 
 FP8BW_API int fp8bw_sync_status(void* stream) {

@@ -39,6 +39,8 @@
 //   warps 2-3   idle
 //   warps 4-11  epilogue: drain the accumulator (warp w: lanes 32*(w%4).., one
 //               128-column half), release it, write bf16 rows.
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -505,6 +507,34 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 }  // namespace
+
+// Scratch of mxfp8_grouped_gemm_noalloc: a fixed array in the library's own
+// device image, so that entry point never allocates.  Every GPU that loads
+// the library holds it until the process exits.  In host code this name is a
+// host-side stand-in, never a device address: launches get the address from
+// static_scratch_address().
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch on the current device, resolved once per
+// device (host code may not use the symbol itself as a device pointer).
+cudaError_t static_scratch_address(void** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
 
 size_t mx_grouped_gemm_workspace_bytes(int kind, int64_t G, int64_t M, int64_t N, int64_t K) {
   const Problem p = make_problem(kind, G, M, N, K);

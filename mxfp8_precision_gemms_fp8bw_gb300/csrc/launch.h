@@ -55,6 +55,11 @@ struct MxGroupedGemmArgs {
   int num_sms;
 };
 size_t mx_grouped_gemm_workspace_bytes(int kind, int64_t G, int64_t M, int64_t N, int64_t K);
+
+// Size of the fixed scratch array behind mxfp8_grouped_gemm_noalloc (16 MiB).
+constexpr size_t kStaticScratchBytes = size_t{16} << 20;
+// Its device address on the current device (resolved once per device).
+cudaError_t static_scratch_address(void** out);
 cudaError_t launch_mx_grouped_gemm(const MxGroupedGemmArgs& args, cudaStream_t st);
 
 cudaError_t launch_selftest_bounded_wait(uint32_t timeout_us, int* status, cudaStream_t st);

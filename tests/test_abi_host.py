@@ -30,7 +30,7 @@ def test_header_declares_the_abi():
         "fp8bw_quant_1x128_row", "fp8bw_quant_1x128_col", "fp8bw_quant_128x128",
         "fp8bw_gemm_fwd", "fp8bw_gemm_dgrad", "fp8bw_gemm_wgrad",
         "mxfp8_quant_1x32_row", "mxfp8_quant_1x32_col", "mxfp8_quant_3d_col", "mxfp8_grouped_gemm",
-        "mxfp8_grouped_gemm_workspace_bytes",
+        "mxfp8_grouped_gemm_workspace_bytes", "mxfp8_grouped_gemm_noalloc",
         "fp8bw_sync_status", "fp8bw_last_error", "fp8bw_selftest_bounded_wait",
     ])
 
@@ -133,3 +133,12 @@ def test_grouped_rejects_small_or_misaligned_workspace(L):
     assert L.mxfp8_grouped_gemm(*args, 128 * P, need - 1, None) == binding.ERR_ARG
     assert "workspace" in binding.last_error()
     assert L.mxfp8_grouped_gemm(*args, 128 * P + 16, need, None) == binding.ERR_ALIGN
+
+
+def test_noalloc_rejects_dims_beyond_its_scratch(L):
+    # DGRAD of 8 experts with K = N = 16384: ~33.6 MB of packed scales > 16 MiB
+    need = L.mxfp8_grouped_gemm_workspace_bytes(1, 8, 16384, 16384, 16384)
+    assert need > binding.NOALLOC_SCRATCH_BYTES
+    rc = L.mxfp8_grouped_gemm_noalloc(1, P, 2 * P, 3 * P, 4 * P, 5 * P, 8, 16384, 16384, 16384, 64 * P, None)
+    assert rc == binding.ERR_SHAPE
+    assert "scratch" in binding.last_error()
