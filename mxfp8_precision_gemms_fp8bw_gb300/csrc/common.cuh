@@ -276,9 +276,12 @@ __device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
   return r;
 }
 
-// Arrive on an mbarrier given by its shared::cluster address (own or peer CTA).
+// Arrive on an mbarrier given by its shared::cluster address (own or peer
+// CTA).  Release at CTA scope: the arrivals this library makes across the pair
+// only publish completed tensor-memory reads (ordered by tcgen05.fence), and a
+// cluster-scope release would stall on every outstanding global store.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // Whole-cluster execution barrier (every thread of both CTAs).

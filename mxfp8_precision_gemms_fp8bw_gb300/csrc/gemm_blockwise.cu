@@ -62,13 +62,12 @@ struct RegSplit {
 struct SharedStorage {
   uint8_t a[STAGES][A_BYTES];  // each stage 1024-byte aligned (swizzle atom)
   uint8_t b[STAGES][B_BYTES];
-  float sb_vec[2][2][128];     // per-row B scales: [column half][buffer][column]
+  float sb_vec[NUM_EPI_WARPS][2][128];  // per-column B scales, private to each promotion warp: [warp][buffer][column]
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t mma_drain;          // used only when unwinding after a timeout
-  uint64_t sb_ready[2];        // per column half: its 4 warps staged this block's B scales
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -112,8 +111,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&sm.tmem_empty[b], NUM_EPI_WARPS);
     }
     mbar_init(&sm.mma_drain, 1);
-    mbar_init(&sm.sb_ready[0], 4);
-    mbar_init(&sm.sb_ready[1], 4);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -224,10 +221,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int half = ew >> 2;                  // column half of the tile
     const int quarter = warp & 3;              // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;       // row of the tile this thread owns
-    const int tid_half = (ew & 3) * 32 + lane; // 0..127 within the column half
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
     int buf = 0;
-    uint32_t tphase = 0, sphase = 0;
+    uint32_t tphase = 0;
     bool alive = true;
     for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
       int mb, nb;
@@ -238,29 +234,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
       for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
 
+      // Scales of the next block are fetched one block ahead.  Per-block B
+      // scale: one value per thread.  Per-column B scale: each lane fetches
+      // four consecutive columns of the warp's 128 (one coalesced 512-byte
+      // row per warp) and stages them in the warp's own shared buffer.
       float sa_next = __ldg(sa + m);
-      float sb_next = kBScale == 0 ? __ldg(sb + (col0 / 128) * sb_ld_nb) : __ldg(sb + col0 + tid_half);
+      float sb_next = kBScale == 0 ? __ldg(sb + (col0 / 128) * sb_ld_nb) : 0.0f;
+      float4 sb4_next = kBScale == 1 ? __ldg(reinterpret_cast<const float4*>(sb + col0) + lane)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
       for (int kb = 0; kb < num_k; ++kb) {
         const float sa_cur = sa_next;
         const float sb_cur = sb_next;
+        if (kBScale == 1) {
+          // The buffer written now was last read two blocks ago; every lane
+          // finished those reads before the previous block's __syncwarp.
+          reinterpret_cast<float4*>(sm.sb_vec[ew][kb & 1])[lane] = sb4_next;
+          __syncwarp();
+        }
         if (kb + 1 < num_k) {
           sa_next = __ldg(sa + static_cast<int64_t>(kb + 1) * sa_ld + m);
-          sb_next = kBScale == 0 ? __ldg(sb + (col0 / 128) * sb_ld_nb + static_cast<int64_t>(kb + 1) * sb_ld_kb)
-                                 : __ldg(sb + static_cast<int64_t>(kb + 1) * sb_ld_kb + col0 + tid_half);
-        }
-        if (kBScale == 1) {
-          // Stage this block's 128 B scales of the column half.  The buffer
-          // written now was last read two blocks ago, before every warp of the
-          // half arrived on the previous block's barrier.
-          sm.sb_vec[half][kb & 1][tid_half] = sb_cur;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.sb_ready[half]);
-          const bool ok = mbar_wait(&sm.sb_ready[half], sphase, ab, status);
-          sphase ^= 1u;
-          if (!ok) {
-            alive = false;
-            break;
-          }
+          if (kBScale == 0)
+            sb_next = __ldg(sb + (col0 / 128) * sb_ld_nb + static_cast<int64_t>(kb + 1) * sb_ld_kb);
+          else
+            sb4_next = __ldg(reinterpret_cast<const float4*>(sb + static_cast<int64_t>(kb + 1) * sb_ld_kb + col0) + lane);
         }
         if (!mbar_wait(&sm.tmem_full[buf], tphase, ab, status)) {
           alive = false;
@@ -276,7 +272,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         constexpr int NG = 8 / NC;
         const float2 fa = make_float2(sa_cur, sa_cur);
         const float2 f2 = kBScale == 0 ? make_float2(sa_cur * sb_cur, sa_cur * sb_cur) : fa;
-        const float* sbv = sm.sb_vec[half][kb & 1];
+        const float* sbv = sm.sb_vec[ew][kb & 1];
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
           uint32_t r[NC][16];
