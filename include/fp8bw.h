@@ -92,6 +92,17 @@ int fp8bw_quant_1x128_row(const fp8bw_bf16* x, int64_t R, int64_t C,
 int fp8bw_quant_1x128_col(const fp8bw_bf16* x, int64_t R, int64_t C,
                           uint8_t* qT, float* s, void* stream);
 
+/* Both 1x128 quantizations of x[R, C] from one read of x: exactly the outputs
+ * of fp8bw_quant_1x128_row (q, s) and of fp8bw_quant_1x128_col (qT, sT).  The
+ * training step needs both for x (forward and grad_weight) and for dy (dgrad
+ * and grad_weight); one pass moves 2 + 2 + 8/128 bytes per element instead
+ * of 2 x (2 + 1 + 4/128).
+ *   x : bf16 [R, C]   q : e4m3 [R, C]   s : fp32 [C/128][R]
+ *                     qT : e4m3 [C, R]  sT : fp32 [R/128][C]
+ * R and C must be positive multiples of 128. */
+int fp8bw_quant_1x128_rowcol(const fp8bw_bf16* x, int64_t R, int64_t C,
+                             uint8_t* q, float* s, uint8_t* qT, float* sT, void* stream);
+
 /* 128x128 weight quantization in one pass ([PR2386] "What I saw": 128x128
  * scaling of one tensor, and "path forward" item 2, a handwritten kernel).
  *   w : bf16 [R, C]   q : e4m3 [R, C]   qT : e4m3 [C, R] or NULL

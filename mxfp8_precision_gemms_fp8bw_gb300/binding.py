@@ -30,6 +30,7 @@ _SIGNATURES = {
     "fp8bw_quant_1x128_row": [_P, _I64, _I64, _P, _P, _P],
     "fp8bw_quant_1x128_col": [_P, _I64, _I64, _P, _P, _P],
     "fp8bw_quant_128x128": [_P, _I64, _I64, _P, _P, _P, _P],
+    "fp8bw_quant_1x128_rowcol": [_P, _I64, _I64, _P, _P, _P, _P, _P],
     "fp8bw_gemm_fwd": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
     "fp8bw_gemm_dgrad": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
     "fp8bw_gemm_wgrad": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
@@ -120,6 +121,12 @@ def fp8bw_quant_1x128_row(x, q, s, stream=None) -> None:
 def fp8bw_quant_1x128_col(x, qT, s, stream=None) -> None:
     R, C = x.shape
     _check(lib().fp8bw_quant_1x128_col(_ptr(x, _BF16, "x"), R, C, _ptr(qT, _U8, "qT"), _ptr(s, _F32, "s"), _stream(stream)))
+
+
+def fp8bw_quant_1x128_rowcol(x, q, s, qT, sT, stream=None) -> None:
+    R, C = x.shape
+    _check(lib().fp8bw_quant_1x128_rowcol(_ptr(x, _BF16, "x"), R, C, _ptr(q, _U8, "q"), _ptr(s, _F32, "s"),
+                                          _ptr(qT, _U8, "qT"), _ptr(sT, _F32, "sT"), _stream(stream)))
 
 
 def fp8bw_quant_128x128(w, q, qT, s, stream=None) -> None:

@@ -152,6 +152,24 @@ FP8BW_API int fp8bw_quant_1x128_col(const fp8bw_bf16* x, int64_t R, int64_t C, u
   return launched(fp8bw::launch_quant_1x128_col(x, R, C, qT, s, as_stream(stream)), "fp8bw_quant_1x128_col");
 }
 
+FP8BW_API int fp8bw_quant_1x128_rowcol(const fp8bw_bf16* x, int64_t R, int64_t C, uint8_t* q, float* s,
+                                       uint8_t* qT, float* sT, void* stream) {
+  const char* name = "fp8bw_quant_1x128_rowcol";
+  if (!x || !q || !s || !qT || !sT) return fail(FP8BW_ERR_NULL, "%s: x, q, s, qT and sT must be non-NULL", name);
+  if (!dim_ok(R, 128) || !dim_ok(C, 128) || R / 128 > 65535)
+    return fail(FP8BW_ERR_SHAPE, "%s: R=%lld and C=%lld must be positive multiples of 128", name, (long long)R,
+                (long long)C);
+  if (!aligned16(x) || !aligned16(q) || !aligned16(s) || !aligned16(qT) || !aligned16(sT))
+    return fail(FP8BW_ERR_ALIGN, "%s: pointers must be 16-byte aligned", name);
+  const int64_t n = R * C;
+  if (overlaps(x, n * 2, q, n) || overlaps(x, n * 2, qT, n) || overlaps(q, n, qT, n) ||
+      overlaps(x, n * 2, s, n / 32) || overlaps(x, n * 2, sT, n / 32) || overlaps(s, n / 32, sT, n / 32))
+    return fail(FP8BW_ERR_LAYOUT, "%s: outputs overlap the input or each other", name);
+  DeviceState* d;
+  if (int rc = current_device(&d)) return rc;
+  return launched(fp8bw::launch_quant_1x128_rowcol(x, R, C, q, s, qT, sT, as_stream(stream)), name);
+}
+
 FP8BW_API int fp8bw_quant_128x128(const fp8bw_bf16* w, int64_t R, int64_t C, uint8_t* q, uint8_t* qT, float* s,
                                   void* stream) {
   if (!w || !q || !s) return fail(FP8BW_ERR_NULL, "fp8bw_quant_128x128: w, q and s must be non-NULL");

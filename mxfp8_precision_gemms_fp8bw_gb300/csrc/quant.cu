@@ -4,9 +4,9 @@
 // All of them are HBM-bound streaming kernels: each element is read once
 // (2 B of bf16) and written once (1 B of e4m3), plus one scale per block.
 // Loads are 16-byte vectors; block maxima are reduced with warp shuffles; the
-// colwise kernels transpose in registers (each thread owns an 8x8 micro-tile
-// and packs e4m3 pairs along the column) so every store is a coalesced
-// 8-byte vector.
+// colwise kernels stage each 128x128 tile in shared memory (coalesced loads,
+// swizzled chunks), then give every thread an 8x8 micro-tile whose columns it
+// packs into e4m3 bytes, so every store is a coalesced 8-byte vector.
 #include "common.cuh"
 #include "launch.h"
 #include "quant_math.cuh"
@@ -121,32 +121,74 @@ __global__ void __launch_bounds__(256) quant_1x128_row_kernel(const uint16_t* __
   if (threadIdx.x < 128) s[static_cast<int64_t>(kb) * R + r0 + threadIdx.x] = s_tile[threadIdx.x];
 }
 
-// ---------------------------------------------------------------- colwise (blockwise and MX)
+// ---------------------------------------------------------------- staged 128x128 tiles
 
-// CTA = 128 rows x 128 columns.  Thread (warp w, lane l) owns the 8x8
-// micro-tile at rows 8*(l & 15) + [0, 8) and columns 8*(2w + (l >> 4)) + [0, 8).
-// A column block spans the 16 lanes of a half-warp (blockwise, 128 rows) or 4
-// of them (MX, 32 rows); its max is reduced with shuffles inside that group.
-// Column j of the micro-tile is quantized into 8 bytes (e4m3 pairs of
-// consecutive rows) and stored at qT[col][row0 .. row0 + 8), so the 16 lanes
-// of a half-warp write 128 contiguous bytes of one qT row.
+// A 128-row x 128-column bf16 tile in shared memory (32 KB) whose 16-byte
+// chunks are XOR-swizzled by the row's 8-row group: chunk k of row r lives at
+// chunk k ^ ((r >> 3) & 15).  Row-major writes (a half-warp per row) and the
+// 8x8 micro-tile reads of the colwise path (16 lanes down one column group)
+// then both run at the minimum number of shared-memory wavefronts.
+struct StagedTile {
+  uint4 chunk[128][16];
+};
+
+__device__ __forceinline__ int swz(int r, int k) { return k ^ ((r >> 3) & 15); }
+
+// Loads rows [r0, r0 + 128) x columns [c0, c0 + 128) of x[R, C] with
+// coalesced 16-byte vectors -- warp w, step i: half-warp h takes row
+// 16w + 2i + h, lane (l & 15) chunk (l & 15) -- into `v` and into the staged
+// tile.  Rows >= R and columns >= C read as zero (C % 8 == 0).
+__device__ __forceinline__ void load_tile(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t r0,
+                                          int64_t c0, StagedTile& t, uint4 (&v)[8]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = lane >> 4, k = lane & 15;
+  const int64_t col = c0 + k * 8;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = warp * 16 + i * 2 + h;
+    v[i] = (r0 + r < R && col < C) ? ld_nc_v4(x + (r0 + r) * C + col) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = warp * 16 + i * 2 + h;
+    t.chunk[r][swz(r, k)] = v[i];
+  }
+}
+
+// Thread (warp w, lane l) of the colwise path owns the 8x8 micro-tile at tile
+// rows 8 * (l & 15) + [0, 8) and columns 8 * (2w + (l >> 4)) + [0, 8).
+__device__ __forceinline__ void read_microtile(const StagedTile& t, uint4 (&v)[8]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rg = lane & 15, cg = warp * 2 + (lane >> 4);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = t.chunk[rg * 8 + i][cg ^ rg];  // swz(8 rg + i, cg)
+}
+
+// Packs column j of the micro-tile (8 consecutive rows, already scaled) into
+// 8 e4m3 bytes and stores them at qT[col][row .. row + 8): the 16 lanes of a
+// half-warp cover 128 contiguous bytes of one qT row.
+__device__ __forceinline__ void store_column8(uint8_t* qT, int64_t R, int64_t col, int64_t row, const float (&qv)[8]) {
+  uint2 o;
+  o.x = cvt_e4m3x2(qv[0], qv[1]) | (cvt_e4m3x2(qv[2], qv[3]) << 16);
+  o.y = cvt_e4m3x2(qv[4], qv[5]) | (cvt_e4m3x2(qv[6], qv[7]) << 16);
+  st_v2(qT + col * R + row, o);
+}
+
+// Colwise quantization of the staged tile: a column block spans the 16 lanes
+// of a half-warp (blockwise, 128 rows) or 4 of them (MX, 32 rows); its max is
+// reduced with shuffles inside that group.
 template <bool kMX>
-__device__ __forceinline__ void colwise_tile(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t r0,
-                                             int64_t c0, uint8_t* __restrict__ qT, float* __restrict__ s,
-                                             uint8_t* __restrict__ e8, int mode) {
+__device__ __forceinline__ void colwise_from_tile(const StagedTile& t, int64_t R, int64_t C, int64_t r0, int64_t c0,
+                                                  uint8_t* __restrict__ qT, float* __restrict__ s,
+                                                  uint8_t* __restrict__ e8, int mode) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rg = lane & 15;
   const int64_t row = r0 + rg * 8;
   const int64_t col = c0 + (warp * 2 + (lane >> 4)) * 8;
-  const bool row_ok = row < R;  // R % 32 == 0, so a 32-row MX block is all in or all out
-  const bool col_ok = col < C;  // C % 8 == 0
+  const bool ok = row < R && col < C;  // R % 32 == 0: a 32-row MX block is all in or all out
 
   uint4 v[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[i] = (row_ok && col_ok) ? ld_nc_v4(x + (row + i) * C + col) : make_uint4(0, 0, 0, 0);
-  }
-
+  read_microtile(t, v);
   float amax[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -161,7 +203,7 @@ __device__ __forceinline__ void colwise_tile(const uint16_t* __restrict__ x, int
     }
     amax[j] = a;
   }
-  if (!(row_ok && col_ok)) return;
+  if (!ok) return;
 
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -179,51 +221,91 @@ __device__ __forceinline__ void colwise_tile(const uint16_t* __restrict__ x, int
       for (int i = 0; i < 8; ++i) qv[i] = div_by_scale(elem8(v[i], j), sc, y);
       if (rg == j) s[(r0 / 128) * C + col + j] = sc;
     }
-    uint2 o;
-    o.x = cvt_e4m3x2(qv[0], qv[1]) | (cvt_e4m3x2(qv[2], qv[3]) << 16);
-    o.y = cvt_e4m3x2(qv[4], qv[5]) | (cvt_e4m3x2(qv[6], qv[7]) << 16);
-    st_v2(qT + (col + j) * R + row, o);
+    store_column8(qT, R, col + j, row, qv);
+  }
+}
+
+// Rowwise 1x128 quantization of the 8 row chunks a thread loaded in
+// load_tile (the half-warp of each row holds its 128 columns).  Writes q and
+// leaves each row's scale in s_rows[row of the tile].
+__device__ __forceinline__ void rowwise_from_regs(const uint4 (&v)[8], int64_t C, int64_t r0, int64_t c0,
+                                                  uint8_t* __restrict__ q, float* s_rows) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = lane >> 4, l16 = lane & 15;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float a = amax8(v[i]);
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    const float sc = blockwise_scale(a);
+    const int rl = warp * 16 + i * 2 + h;
+    st_v2(q + (r0 + rl) * C + c0 + l16 * 8, quant8_div(v[i], sc, __frcp_rn(sc)));
+    if (l16 == 0) s_rows[rl] = sc;
   }
 }
 
 __global__ void __launch_bounds__(256) quant_1x128_col_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C,
                                                               uint8_t* __restrict__ qT, float* __restrict__ s) {
-  colwise_tile<false>(x, R, C, static_cast<int64_t>(blockIdx.y) * 128, static_cast<int64_t>(blockIdx.x) * 128, qT, s,
-                      nullptr, 0);
+  __shared__ StagedTile tile;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128, c0 = static_cast<int64_t>(blockIdx.x) * 128;
+  uint4 v[8];
+  load_tile(x, R, C, r0, c0, tile, v);
+  __syncthreads();
+  colwise_from_tile<false>(tile, R, C, r0, c0, qT, s, nullptr, 0);
+}
+
+// Both 1x128 quantizations of one tile from a single read of x: rowwise from
+// the loaded registers, colwise from the staged tile.
+__global__ void __launch_bounds__(256) quant_1x128_rowcol_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C,
+                                                                 uint8_t* __restrict__ q, float* __restrict__ s,
+                                                                 uint8_t* __restrict__ qT, float* __restrict__ sT) {
+  __shared__ StagedTile tile;
+  __shared__ float s_rows[128];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128, c0 = static_cast<int64_t>(blockIdx.x) * 128;
+  uint4 v[8];
+  load_tile(x, R, C, r0, c0, tile, v);
+  rowwise_from_regs(v, C, r0, c0, q, s_rows);
+  __syncthreads();
+  if (threadIdx.x < 128) s[static_cast<int64_t>(blockIdx.x) * R + r0 + threadIdx.x] = s_rows[threadIdx.x];
+  colwise_from_tile<false>(tile, R, C, r0, c0, qT, sT, nullptr, 0);
 }
 
 // grid.z = expert index for the 3D case (per-expert strides passed in).
 __global__ void __launch_bounds__(256) mx_quant_col_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C,
                                                            uint8_t* __restrict__ qT, uint8_t* __restrict__ e8,
                                                            int mode) {
+  __shared__ StagedTile tile;
   const int64_t g = blockIdx.z;
-  colwise_tile<true>(x + g * R * C, R, C, static_cast<int64_t>(blockIdx.y) * 128,
-                     static_cast<int64_t>(blockIdx.x) * 128, qT + g * R * C, nullptr, e8 + g * C * (R / 32), mode);
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128, c0 = static_cast<int64_t>(blockIdx.x) * 128;
+  uint4 v[8];
+  load_tile(x + g * R * C, R, C, r0, c0, tile, v);
+  __syncthreads();
+  colwise_from_tile<true>(tile, R, C, r0, c0, qT + g * R * C, nullptr, e8 + g * C * (R / 32), mode);
 }
 
 // ---------------------------------------------------------------- 128x128
 
-// Same micro-tile mapping as the colwise kernels; one scale for the whole
-// CTA tile.  Writes q row-major and, when requested, qT.
+// One scale for the whole tile: the max of the loaded registers reduced over
+// the CTA; q is written row-major from registers (a half-warp per 128-byte row
+// segment), qT from the staged tile's micro-tiles.
 __global__ void __launch_bounds__(256) quant_128x128_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C,
                                                             uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
                                                             float* __restrict__ s, int64_t s_ld) {
+  __shared__ StagedTile tile;
   __shared__ float warp_max[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128, c0 = static_cast<int64_t>(blockIdx.x) * 128;
-  const int64_t row = r0 + (lane & 15) * 8;
-  const int64_t col = c0 + (warp * 2 + (lane >> 4)) * 8;
-
   uint4 v[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = ld_nc_v4(x + (row + i) * C + col);
+  load_tile(x, R, C, r0, c0, tile, v);
   float a = 0.0f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) a = fmaxf(a, amax8(v[i]));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
   if (lane == 0) warp_max[warp] = a;
-  __syncthreads();
+  __syncthreads();  // also publishes the staged tile
   a = warp_max[0];
 #pragma unroll
   for (int w = 1; w < 8; ++w) a = fmaxf(a, warp_max[w]);
@@ -231,18 +313,23 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const uint16_t* __re
   const float y = __frcp_rn(sc);
   if (threadIdx.x == 0) s[blockIdx.y * s_ld + blockIdx.x] = sc;
 
+  const int h = lane >> 4, l16 = lane & 15;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) st_v2(q + (row + i) * C + col, quant8_div(v[i], sc, y));
+  for (int i = 0; i < 8; ++i) {
+    const int64_t r = r0 + warp * 16 + i * 2 + h;
+    st_v2(q + r * C + c0 + l16 * 8, quant8_div(v[i], sc, y));
+  }
   if (qT != nullptr) {
+    const int rg = lane & 15;
+    const int64_t row = r0 + rg * 8;
+    const int64_t col = c0 + (warp * 2 + (lane >> 4)) * 8;
+    read_microtile(tile, v);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       float qv[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) qv[i] = div_by_scale(elem8(v[i], j), sc, y);
-      uint2 o;
-      o.x = cvt_e4m3x2(qv[0], qv[1]) | (cvt_e4m3x2(qv[2], qv[3]) << 16);
-      o.y = cvt_e4m3x2(qv[4], qv[5]) | (cvt_e4m3x2(qv[6], qv[7]) << 16);
-      st_v2(qT + (col + j) * R + row, o);
+      store_column8(qT, R, col + j, row, qv);
     }
   }
 }
@@ -290,6 +377,13 @@ cudaError_t launch_quant_1x128_row(const uint16_t* x, int64_t R, int64_t C, uint
 cudaError_t launch_quant_1x128_col(const uint16_t* x, int64_t R, int64_t C, uint8_t* qT, float* s, cudaStream_t st) {
   dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(R / 128));
   quant_1x128_col_kernel<<<grid, 256, 0, st>>>(x, R, C, qT, s);
+  return finish();
+}
+
+cudaError_t launch_quant_1x128_rowcol(const uint16_t* x, int64_t R, int64_t C, uint8_t* q, float* s, uint8_t* qT,
+                                      float* sT, cudaStream_t st) {
+  dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(R / 128));
+  quant_1x128_rowcol_kernel<<<grid, 256, 0, st>>>(x, R, C, q, s, qT, sT);
   return finish();
 }
 

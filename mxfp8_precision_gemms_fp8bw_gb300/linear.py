@@ -6,10 +6,12 @@ and whose backward is two; PR #2386 (description) gives the block shapes.
 This module only orders the library calls and allocates their outputs with
 torch; every quantization and GEMM runs in libfp8bw's kernels.
 
-Forward   : x -> 1x128 rowwise (q_x, s_x); W -> 128x128 (q_W, q_W^T, s_W);
-            y = gemm_fwd(q_x, s_x, q_W, s_W)
-Backward  : dy -> 1x128 rowwise (q_dy, s_dy) -> dx = gemm_dgrad(q_dy, s_dy, q_W^T, s_W)
-            dy, x -> 1x128 colwise along tokens -> dW = gemm_wgrad(...)
+Forward   : x -> 1x128 rowwise and colwise in one pass (q_x, s_x, q_x^T, s_x^T);
+            W -> 128x128 (q_W, q_W^T, s_W); y = gemm_fwd(q_x, s_x, q_W, s_W).
+            The colwise x codes (1 byte per element) are kept for backward
+            instead of the bf16 x.
+Backward  : dy -> 1x128 rowwise and colwise in one pass;
+            dx = gemm_dgrad(q_dy, s_dy, q_W^T, s_W); dW = gemm_wgrad(q_dy^T, s_dy^T, q_x^T, s_x^T)
 """
 from __future__ import annotations
 
@@ -34,28 +36,33 @@ def quantize_weight(w: torch.Tensor, stream=None) -> QuantizedWeight:
 
 
 def forward(x: torch.Tensor, wq: QuantizedWeight, stream=None):
-    """y = x W^T with x quantized 1x128 rowwise.  Returns y and (q_x, s_x)."""
+    """y = x W^T.  Returns y and the colwise codes of x (q_x^T, s_x^T) that
+    the backward pass needs, both quantizations coming from one read of x."""
     M, K = x.shape
     N = wq.q.shape[0]
     xq, xs = B.alloc_quant_1x128_row(x)
-    B.fp8bw_quant_1x128_row(x, xq, xs, stream)
+    xqT, xsT = B.alloc_quant_1x128_col(x)
+    B.fp8bw_quant_1x128_rowcol(x, xq, xs, xqT, xsT, stream)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     B.fp8bw_gemm_fwd(xq, xs, wq.q, wq.s, y, stream)
-    return y, (xq, xs)
+    return y, (xqT, xsT)
 
 
-def backward(dy: torch.Tensor, x: torch.Tensor, wq: QuantizedWeight, stream=None):
-    """dx = dy W and dW = dy^T x.  Returns (dx, dW)."""
+def backward(dy: torch.Tensor, x_col, wq: QuantizedWeight, stream=None):
+    """dx = dy W and dW = dy^T x.  x_col is (q_x^T, s_x^T) from forward, or
+    the bf16 x itself (then quantized colwise here).  Returns (dx, dW)."""
     M, N = dy.shape
-    K = x.shape[1]
+    if isinstance(x_col, torch.Tensor):
+        xqT, xsT = B.alloc_quant_1x128_col(x_col)
+        B.fp8bw_quant_1x128_col(x_col, xqT, xsT, stream)
+    else:
+        xqT, xsT = x_col
+    K = xqT.shape[0]
     dyq, dys = B.alloc_quant_1x128_row(dy)
-    B.fp8bw_quant_1x128_row(dy, dyq, dys, stream)
+    dyqT, dysT = B.alloc_quant_1x128_col(dy)
+    B.fp8bw_quant_1x128_rowcol(dy, dyq, dys, dyqT, dysT, stream)
     dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device)
     B.fp8bw_gemm_dgrad(dyq, dys, wq.qT, wq.s, dx, stream)
-    dyqT, dysT = B.alloc_quant_1x128_col(dy)
-    B.fp8bw_quant_1x128_col(dy, dyqT, dysT, stream)
-    xqT, xsT = B.alloc_quant_1x128_col(x)
-    B.fp8bw_quant_1x128_col(x, xqT, xsT, stream)
     dW = torch.empty((N, K), dtype=torch.bfloat16, device=dy.device)
     B.fp8bw_gemm_wgrad(dyqT, dysT, xqT, xsT, dW, stream)
     return dx, dW
@@ -65,15 +72,14 @@ class _Float8BlockwiseLinearFn(torch.autograd.Function):
     @staticmethod
     def forward(ctx, x, w):
         wq = quantize_weight(w)
-        y, _ = forward(x, wq)
-        ctx.save_for_backward(x)
+        y, x_col = forward(x, wq)
+        ctx.x_col = x_col
         ctx.wq = wq
         return y
 
     @staticmethod
     def backward(ctx, dy):
-        (x,) = ctx.saved_tensors
-        dx, dW = backward(dy.contiguous(), x, ctx.wq)
+        dx, dW = backward(dy.contiguous(), ctx.x_col, ctx.wq)
         return dx, dW
 
 
@@ -155,8 +161,8 @@ class BlockwiseLinearWorkspace:
     Inputs: x [M, K], w [N, K], dy [M, N] bf16 on the workspace's device.
     """
 
-    NAMES = ("quant_1x128_row(x)", "quant_128x128(W)", "gemm_fwd", "quant_1x128_row(dy)", "gemm_dgrad",
-             "quant_1x128_col(dy)", "quant_1x128_col(x)", "gemm_wgrad")
+    NAMES = ("quant_1x128_rowcol(x)", "quant_128x128(W)", "gemm_fwd", "quant_1x128_rowcol(dy)", "gemm_dgrad",
+             "gemm_wgrad")
 
     def __init__(self, M: int, N: int, K: int, device="cuda"):
         self.M, self.N, self.K = M, N, K
@@ -174,13 +180,13 @@ class BlockwiseLinearWorkspace:
 
     def kernels(self, x, w, dy, stream=None):
         return [
-            ("quant_1x128_row(x)", lambda: B.fp8bw_quant_1x128_row(x, self.xq, self.xs, stream)),
+            ("quant_1x128_rowcol(x)",
+             lambda: B.fp8bw_quant_1x128_rowcol(x, self.xq, self.xs, self.xqT, self.xsT, stream)),
             ("quant_128x128(W)", lambda: B.fp8bw_quant_128x128(w, self.wq, self.wqT, self.ws, stream)),
             ("gemm_fwd", lambda: B.fp8bw_gemm_fwd(self.xq, self.xs, self.wq, self.ws, self.y, stream)),
-            ("quant_1x128_row(dy)", lambda: B.fp8bw_quant_1x128_row(dy, self.dyq, self.dys, stream)),
+            ("quant_1x128_rowcol(dy)",
+             lambda: B.fp8bw_quant_1x128_rowcol(dy, self.dyq, self.dys, self.dyqT, self.dysT, stream)),
             ("gemm_dgrad", lambda: B.fp8bw_gemm_dgrad(self.dyq, self.dys, self.wqT, self.ws, self.dx, stream)),
-            ("quant_1x128_col(dy)", lambda: B.fp8bw_quant_1x128_col(dy, self.dyqT, self.dysT, stream)),
-            ("quant_1x128_col(x)", lambda: B.fp8bw_quant_1x128_col(x, self.xqT, self.xsT, stream)),
             ("gemm_wgrad", lambda: B.fp8bw_gemm_wgrad(self.dyqT, self.dysT, self.xqT, self.xsT, self.dW, stream)),
         ]
 
@@ -192,15 +198,14 @@ class BlockwiseLinearWorkspace:
     def algorithmic(self):
         """Per-kernel algorithmic work: bytes moved (quantizers) or flops (GEMMs)."""
         M, N, K = self.M, self.N, self.K
-        row = lambda r, c: r * c * 3 + 4 * r * c // 128  # noqa: E731  bf16 in, e4m3 out, one fp32 per 128
+        # bf16 in once; e4m3 out twice (rowwise and colwise); one fp32 per 128 each way
+        rowcol = lambda r, c: r * c * 4 + 2 * 4 * r * c // 128  # noqa: E731
         return {
-            "quant_1x128_row(x)": ("bytes", row(M, K)),
+            "quant_1x128_rowcol(x)": ("bytes", rowcol(M, K)),
             "quant_128x128(W)": ("bytes", N * K * 4 + 4 * (N // 128) * (K // 128)),
             "gemm_fwd": ("flops", 2 * M * N * K),
-            "quant_1x128_row(dy)": ("bytes", row(M, N)),
+            "quant_1x128_rowcol(dy)": ("bytes", rowcol(M, N)),
             "gemm_dgrad": ("flops", 2 * M * N * K),
-            "quant_1x128_col(dy)": ("bytes", row(M, N)),
-            "quant_1x128_col(x)": ("bytes", row(M, K)),
             "gemm_wgrad": ("flops", 2 * M * N * K),
         }
 

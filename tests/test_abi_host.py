@@ -27,7 +27,7 @@ def _declared_functions():
 def test_header_declares_the_abi():
     names = _declared_functions()
     assert names == sorted([
-        "fp8bw_quant_1x128_row", "fp8bw_quant_1x128_col", "fp8bw_quant_128x128",
+        "fp8bw_quant_1x128_row", "fp8bw_quant_1x128_col", "fp8bw_quant_128x128", "fp8bw_quant_1x128_rowcol",
         "fp8bw_gemm_fwd", "fp8bw_gemm_dgrad", "fp8bw_gemm_wgrad",
         "mxfp8_quant_1x32_row", "mxfp8_quant_1x32_col", "mxfp8_quant_3d_col", "mxfp8_grouped_gemm",
         "mxfp8_grouped_gemm_workspace_bytes", "mxfp8_grouped_gemm_noalloc",

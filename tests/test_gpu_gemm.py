@@ -133,3 +133,19 @@ def test_full_size_dense_sampled():
     a = oracle.dequant_1x128_row(*dyT)
     b = oracle.dequant_1x128_row(*xT)
     assert gemm_max_err(dW[np.ix_(ns, ks)], a @ b.T, a, b) <= TOL
+
+
+def test_float8_blockwise_linear_module_autograd():
+    # The nn.Linear replacement of PR #4295: forward and backward through autograd.
+    t = inputs.tiny()
+    layer = L.Float8BlockwiseLinear(512, 512, device="cuda")
+    with torch.no_grad():
+        layer.weight.copy_(t.w.cuda())
+    x = t.x.cuda().requires_grad_(True)
+    y = layer(x)
+    y.backward(t.dy.cuda())
+    torch.cuda.synchronize()
+    yr, dxr, dWr, d = oracle_linear(t.x, t.w, t.dy)
+    assert gemm_max_err(f32(y), yr, d["x"], d["w"]) <= TOL
+    assert gemm_max_err(f32(x.grad), dxr, d["dy"], d["w"].T) <= TOL
+    assert gemm_max_err(f32(layer.weight.grad), dWr, d["dyT"], d["xT"]) <= TOL

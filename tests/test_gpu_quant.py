@@ -64,6 +64,21 @@ def test_1x128_col_bit_exact(R, C, seed):
     assert np.array_equal(bits(s), bits(so))
 
 
+@pytest.mark.parametrize("R,C,seed", [(128, 128, 11), (256, 512, 12), (640, 384, 13), (1152, 896, 14)])
+def test_1x128_rowcol_bit_exact(R, C, seed):
+    # one read of x, both outputs: identical to the separate row and col quantizers
+    x = adversarial_bf16(R, C, seed) if seed % 2 else transpose_adversarial(R, C, seed)
+    xd = x.cuda()
+    q, s = B.alloc_quant_1x128_row(xd)
+    qT, sT = B.alloc_quant_1x128_col(xd)
+    B.fp8bw_quant_1x128_rowcol(xd, q, s, qT, sT)
+    B.fp8bw_sync_status()
+    qo, so = oracle.quant_1x128_row(f32(x))
+    qTo, sTo = oracle.quant_1x128_col(f32(x))
+    assert np.array_equal(u8(q), qo) and np.array_equal(bits(s), bits(so))
+    assert np.array_equal(u8(qT), qTo) and np.array_equal(bits(sT), bits(sTo))
+
+
 @pytest.mark.parametrize("R,C,seed", [(128, 128, 8), (384, 640, 9), (512, 384, 10)])
 def test_128x128_bit_exact(R, C, seed):
     x = adversarial_bf16(R, C, seed)
@@ -149,7 +164,11 @@ def test_full_size_dense_row_and_col_quant(dense):
         B.fp8bw_quant_1x128_row(td, q, s)
         qT, sT = B.alloc_quant_1x128_col(td)
         B.fp8bw_quant_1x128_col(td, qT, sT)
+        q2, s2 = B.alloc_quant_1x128_row(td)
+        qT2, sT2 = B.alloc_quant_1x128_col(td)
+        B.fp8bw_quant_1x128_rowcol(td, q2, s2, qT2, sT2)
         B.fp8bw_sync_status()
+        assert torch.equal(q, q2) and torch.equal(s, s2) and torch.equal(qT, qT2) and torch.equal(sT, sT2)
         q, s, qT, sT = u8(q), s.cpu().numpy(), u8(qT), sT.cpu().numpy()
         tf = f32(t)
         for r0, r1 in _chunks(tf.shape[0], 2048):
