@@ -3,10 +3,16 @@
 //
 // All of them are HBM-bound streaming kernels: each element is read once
 // (2 B of bf16) and written once (1 B of e4m3), plus one scale per block.
-// Loads are 16-byte vectors; block maxima are reduced with warp shuffles; the
-// colwise kernels stage each 128x128 tile in shared memory (coalesced loads,
-// swizzled chunks), then give every thread an 8x8 micro-tile whose columns it
-// packs into e4m3 bytes, so every store is a coalesced 8-byte vector.
+// Loads are 16-byte vectors.  Block maxima are taken on packed bf16 pairs
+// (max.xorsign.abs.bf16x2, exact) and reduced with warp shuffles; the
+// blockwise division runs two elements per instruction (f32x2 FMUL2/FFMA2).
+// The colwise-type kernels are persistent: each CTA streams 128x128 tiles
+// through a ring of shared-memory buffers filled by cp.async (coalesced row
+// loads, swizzled 16-byte chunks) and gives every thread an 8x8 micro-tile
+// whose columns it packs into e4m3 bytes, so every store is a coalesced
+// 8-byte vector.
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 #include "quant_math.cuh"
@@ -35,42 +41,62 @@ __device__ __forceinline__ float pow2_neg(int E) {
   return be > 0 ? __uint_as_float(static_cast<uint32_t>(be) << 23) : __uint_as_float(0x00400000u);
 }
 
-__device__ __forceinline__ float amax8(const uint4& v) {
-  float a = fabsf(bf16lo_to_f32(v.x));
-  a = fmaxf(a, fabsf(bf16hi_to_f32(v.x)));
-  a = fmaxf(a, fabsf(bf16lo_to_f32(v.y)));
-  a = fmaxf(a, fabsf(bf16hi_to_f32(v.y)));
-  a = fmaxf(a, fabsf(bf16lo_to_f32(v.z)));
-  a = fmaxf(a, fabsf(bf16hi_to_f32(v.z)));
-  a = fmaxf(a, fabsf(bf16lo_to_f32(v.w)));
-  a = fmaxf(a, fabsf(bf16hi_to_f32(v.w)));
-  return a;
+// max(|a|, |b|) in each bf16 half (exact); the result's sign bits are
+// meaningless (max.xorsign.abs sets them to the XOR of the inputs' signs).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int k) { return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w; }
+
+// |x| max of 8 packed bf16: even elements in the low half, odd in the high.
+__device__ __forceinline__ uint32_t absmax8(const uint4& v) {
+  return absmax_bf16x2(absmax_bf16x2(v.x, v.y), absmax_bf16x2(v.z, v.w));
+}
+
+// Two such partial maxes (of rows a and b) folded into one word: row a's max
+// in the low half, row b's in the high half.
+__device__ __forceinline__ uint32_t fold_pair(uint32_t ma, uint32_t mb) {
+  return absmax_bf16x2(__byte_perm(ma, mb, 0x5410), __byte_perm(ma, mb, 0x7632));
+}
+
+__device__ __forceinline__ uint32_t shfl_absmax(uint32_t m, int lane_mask) {
+  return absmax_bf16x2(m, __shfl_xor_sync(0xffffffffu, m, lane_mask));
+}
+
+// Value c (0..7) of four packed maxes, as a non-negative fp32 (exact).
+__device__ __forceinline__ float unpack_amax(const uint32_t (&m)[4], int c) {
+  const uint32_t w = (c & 4) ? ((c & 2) ? m[3] : m[2]) : ((c & 2) ? m[1] : m[0]);
+  return __uint_as_float((c & 1) ? (w & 0x7FFF0000u) : (w & 0x7FFFu) << 16);
 }
 
 // Element j (0..7) of 8 packed bf16.
 __device__ __forceinline__ float elem8(const uint4& v, int j) {
-  const uint32_t w = j < 2 ? v.x : j < 4 ? v.y : j < 6 ? v.z : v.w;
+  const uint32_t w = word(v, j >> 1);
   return (j & 1) ? bf16hi_to_f32(w) : bf16lo_to_f32(w);
 }
 
-// Eight e4m3 codes of fl32(x/s) packed little-endian; y = RN(1/s).
-__device__ __forceinline__ uint2 quant8_div(const uint4& v, float s, float y) {
-  uint2 o;
-  o.x = cvt_e4m3x2(div_by_scale(bf16lo_to_f32(v.x), s, y), div_by_scale(bf16hi_to_f32(v.x), s, y)) |
-        (cvt_e4m3x2(div_by_scale(bf16lo_to_f32(v.y), s, y), div_by_scale(bf16hi_to_f32(v.y), s, y)) << 16);
-  o.y = cvt_e4m3x2(div_by_scale(bf16lo_to_f32(v.z), s, y), div_by_scale(bf16hi_to_f32(v.z), s, y)) |
-        (cvt_e4m3x2(div_by_scale(bf16lo_to_f32(v.w), s, y), div_by_scale(bf16hi_to_f32(v.w), s, y)) << 16);
-  return o;
+__device__ __forceinline__ float2 pair_of_word(uint32_t w) { return make_float2(bf16lo_to_f32(w), bf16hi_to_f32(w)); }
+
+// Eight e4m3 codes of fl32(x / s) packed little-endian; ny = neg_recip(s).
+__device__ __forceinline__ uint2 quant8_div(const uint4& v, float s, float ny) {
+  const float2 S = make_float2(s, s), NY = make_float2(ny, ny);
+  const float2 a = neg_div_by_scale2(pair_of_word(v.x), S, NY);
+  const float2 b = neg_div_by_scale2(pair_of_word(v.y), S, NY);
+  const float2 c = neg_div_by_scale2(pair_of_word(v.z), S, NY);
+  const float2 d = neg_div_by_scale2(pair_of_word(v.w), S, NY);
+  return make_uint2(e4m3x4_from_neg(a, b), e4m3x4_from_neg(c, d));
 }
 
 // Eight e4m3 codes of x * m (MX: m = 2^-E, an exact power of two).
 __device__ __forceinline__ uint2 quant8_mul(const uint4& v, float m) {
-  uint2 o;
-  o.x = cvt_e4m3x2(bf16lo_to_f32(v.x) * m, bf16hi_to_f32(v.x) * m) |
-        (cvt_e4m3x2(bf16lo_to_f32(v.y) * m, bf16hi_to_f32(v.y) * m) << 16);
-  o.y = cvt_e4m3x2(bf16lo_to_f32(v.z) * m, bf16hi_to_f32(v.z) * m) |
-        (cvt_e4m3x2(bf16lo_to_f32(v.w) * m, bf16hi_to_f32(v.w) * m) << 16);
-  return o;
+  const float2 M = make_float2(m, m);
+  const float2 a = __fmul2_rn(pair_of_word(v.x), M), b = __fmul2_rn(pair_of_word(v.y), M);
+  const float2 c = __fmul2_rn(pair_of_word(v.z), M), d = __fmul2_rn(pair_of_word(v.w), M);
+  return make_uint2(__byte_perm(cvt_e4m3x2(a.x, a.y), cvt_e4m3x2(b.x, b.y), 0x5410),
+                    __byte_perm(cvt_e4m3x2(c.x, c.y), cvt_e4m3x2(d.x, d.y), 0x5410));
 }
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
@@ -87,45 +113,54 @@ __device__ __forceinline__ void st_v2(void* p, uint2 v) {
 
 // ---------------------------------------------------------------- 1x128 rowwise
 
-// CTA = 128 rows x one 128-column block.  Warp w owns rows [16w, 16w + 16);
-// per step each half-warp takes one row and lane (l & 15) columns
-// [8(l & 15), 8(l & 15) + 8).  All eight 16-byte loads are issued first.
+// Rowwise 1x128 quantization of the eight row chunks a thread holds: thread
+// (warp w, lane l) has rows r0 + 16w + 2i + (l >> 4), i = 0..7, columns
+// c0 + 8 (l & 15) + [0, 8).  The 16 lanes of a row reduce its max (two rows
+// per packed word); lane i of each half-warp then derives row i's scale and
+// reciprocal once, and shuffles hand them to the other lanes.  Writes q and
+// the row scales s[c0 / 128][row].
+__device__ __forceinline__ void rowwise_quant(const uint4 (&v)[8], int64_t R, int64_t C, int64_t r0, int64_t c0,
+                                              uint8_t* __restrict__ q, float* __restrict__ s) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = lane >> 4, l16 = lane & 15;
+  uint32_t m[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) m[p] = fold_pair(absmax8(v[2 * p]), absmax8(v[2 * p + 1]));
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) m[p] = shfl_absmax(m[p], o);
+  }
+  const float sc = blockwise_scale(unpack_amax(m, l16 & 7));
+  const float ny = neg_recip(sc);
+  const int64_t rbase = r0 + warp * 16 + h;
+  if (l16 < 8) s[(c0 / 128) * R + rbase + 2 * l16] = sc;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float si = __shfl_sync(0xffffffffu, sc, (lane & 16) | i);
+    const float nyi = __shfl_sync(0xffffffffu, ny, (lane & 16) | i);
+    st_v2(q + (rbase + 2 * i) * C + c0 + l16 * 8, quant8_div(v[i], si, nyi));
+  }
+}
+
+// CTA = 128 rows x one 128-column block, all eight 16-byte loads per thread
+// issued up front.
 __global__ void __launch_bounds__(256) quant_1x128_row_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C,
                                                               uint8_t* __restrict__ q, float* __restrict__ s) {
-  __shared__ float s_tile[128];
-  const int kb = blockIdx.x;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128, r0 = static_cast<int64_t>(blockIdx.y) * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int half = lane >> 4, l16 = lane & 15;
-  const int64_t col = static_cast<int64_t>(kb) * 128 + l16 * 8;
-
+  const int64_t col = c0 + (lane & 15) * 8;
   uint4 v[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int64_t r = r0 + warp * 16 + i * 2 + half;
-    v[i] = ld_nc_v4(x + r * C + col);
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float a = amax8(v[i]);
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    const float sc = blockwise_scale(a);
-    const int rl = warp * 16 + i * 2 + half;
-    st_v2(q + (r0 + rl) * C + col, quant8_div(v[i], sc, __frcp_rn(sc)));
-    if (l16 == 0) s_tile[rl] = sc;
-  }
-  __syncthreads();
-  if (threadIdx.x < 128) s[static_cast<int64_t>(kb) * R + r0 + threadIdx.x] = s_tile[threadIdx.x];
+  for (int i = 0; i < 8; ++i) v[i] = ld_nc_v4(x + (r0 + warp * 16 + i * 2 + (lane >> 4)) * C + col);
+  rowwise_quant(v, R, C, r0, c0, q, s);
 }
 
 // ---------------------------------------------------------------- staged 128x128 tiles
 
 // A 128-row x 128-column bf16 tile in shared memory (32 KB) whose 16-byte
 // chunks are XOR-swizzled by the row's 8-row group: chunk k of row r lives at
-// chunk k ^ ((r >> 3) & 15).  Row-major writes (a half-warp per row) and the
+// chunk k ^ ((r >> 3) & 15).  Row-major accesses (a half-warp per row) and the
 // 8x8 micro-tile reads of the colwise path (16 lanes down one column group)
 // then both run at the minimum number of shared-memory wavefronts.
 struct StagedTile {
@@ -134,25 +169,131 @@ struct StagedTile {
 
 __device__ __forceinline__ int swz(int r, int k) { return k ^ ((r >> 3) & 15); }
 
-// Loads rows [r0, r0 + 128) x columns [c0, c0 + 128) of x[R, C] with
-// coalesced 16-byte vectors -- warp w, step i: half-warp h takes row
-// 16w + 2i + h, lane (l & 15) chunk (l & 15) -- into `v` and into the staged
-// tile.  Rows >= R and columns >= C read as zero (C % 8 == 0).
-__device__ __forceinline__ void load_tile(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t r0,
-                                          int64_t c0, StagedTile& t, uint4 (&v)[8]) {
+// The colwise-type quantizers are persistent: each CTA walks tiles
+// blockIdx.x, blockIdx.x + gridDim.x, ... through a ring of kQuantStages
+// staged tiles filled by cp.async, so the loads of the next tiles are in
+// flight while the current one is quantized and stored.
+#ifndef FP8BW_QSTAGES
+#define FP8BW_QSTAGES 3
+#endif
+#ifndef FP8BW_QCTAS
+#define FP8BW_QCTAS 2
+#endif
+constexpr int kQuantStages = FP8BW_QSTAGES;
+constexpr int kQuantCtasPerSm = FP8BW_QCTAS;
+constexpr size_t kQuantSmem = kQuantStages * sizeof(StagedTile);
+
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Issues the copy of rows [r0, r0 + 128) x columns [c0, c0 + 128) of x[R, C]
+// into `t`: warp w, step i, half-warp h takes row 16w + 2i + h, lane (l & 15)
+// chunk (l & 15) -- two 256-byte row segments per warp instruction.  Rows >= R
+// and columns >= C are zero-filled (C % 8 == 0), reading nothing.
+__device__ __forceinline__ void fetch_tile(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t r0,
+                                           int64_t c0, StagedTile& t) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = lane >> 4, k = lane & 15;
   const int64_t col = c0 + k * 8;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int r = warp * 16 + i * 2 + h;
-    v[i] = (r0 + r < R && col < C) ? ld_nc_v4(x + (r0 + r) * C + col) : make_uint4(0, 0, 0, 0);
+    const bool ok = r0 + r < R && col < C;
+    cp_async_16(&t.chunk[r][swz(r, k)], ok ? x + (r0 + r) * C + col : x, ok ? 16u : 0u);
   }
+}
+
+// The thread's 8 row chunks of the staged tile, in the mapping of fetch_tile.
+__device__ __forceinline__ void read_rows(const StagedTile& t, uint4 (&v)[8]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = lane >> 4, k = lane & 15;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int r = warp * 16 + i * 2 + h;
-    t.chunk[r][swz(r, k)] = v[i];
+    v[i] = t.chunk[r][swz(r, k)];
   }
+}
+
+// Tiles of a stack of G matrices [R, C]: tile t -> matrix g, row band rb,
+// column block cb (column blocks fastest).
+struct TileSpace {
+  int64_t R, C;
+  int tiles_c, tiles_r, G;
+};
+
+struct TileCursor {
+  int g, rb, cb;
+};
+
+// A stride of whole tiles split into column blocks, row bands and matrices.
+struct TileStep {
+  int dcb, drb, dg;
+};
+
+__device__ __forceinline__ TileCursor cursor_at(const TileSpace& ts, int64_t t) {
+  const int64_t per_matrix = static_cast<int64_t>(ts.tiles_c) * ts.tiles_r;
+  TileCursor c;
+  c.g = static_cast<int>(t / per_matrix);
+  const int64_t u = t - c.g * per_matrix;
+  c.rb = static_cast<int>(u / ts.tiles_c);
+  c.cb = static_cast<int>(u - static_cast<int64_t>(c.rb) * ts.tiles_c);
+  return c;
+}
+
+__device__ __forceinline__ TileStep step_of(const TileSpace& ts, int stride) {
+  const int rest = stride / ts.tiles_c;
+  return TileStep{stride % ts.tiles_c, rest % ts.tiles_r, rest / ts.tiles_r};
+}
+
+// Moves the cursor `d` tiles on with carries instead of divisions.
+__device__ __forceinline__ void advance(TileCursor& c, const TileSpace& ts, const TileStep& d) {
+  c.cb += d.dcb;
+  int carry = c.cb >= ts.tiles_c;
+  if (carry) c.cb -= ts.tiles_c;
+  c.rb += d.drb + carry;
+  carry = c.rb >= ts.tiles_r;
+  if (carry) c.rb -= ts.tiles_r;
+  c.g += d.dg + carry;
+}
+
+// Runs body(tile, g, r0, c0) on the tiles blockIdx.x, blockIdx.x + gridDim.x,
+// ..., kQuantStages - 1 tiles ahead of the loads.  Each iteration waits for
+// its own tile's copies (cp.async.wait_group), then a CTA barrier makes them
+// visible to all threads and guarantees that everyone has left the previous
+// tile, whose buffer the next prefetch overwrites.
+template <typename Body>
+__device__ __forceinline__ void for_each_staged_tile(const uint16_t* __restrict__ x, const TileSpace& ts,
+                                                     StagedTile* ring, Body&& body) {
+  const TileStep d = step_of(ts, gridDim.x);
+  TileCursor pre = cursor_at(ts, blockIdx.x);
+  TileCursor cur = pre;
+  const int64_t matrix = ts.R * ts.C;
+#pragma unroll
+  for (int s = 0; s < kQuantStages - 1; ++s) {
+    if (pre.g < ts.G) fetch_tile(x + pre.g * matrix, ts.R, ts.C, pre.rb * 128ll, pre.cb * 128ll, ring[s]);
+    cp_async_commit();
+    advance(pre, ts, d);
+  }
+  int stage = 0;
+  while (cur.g < ts.G) {
+    cp_async_wait<kQuantStages - 2>();
+    __syncthreads();
+    const int ahead = stage == 0 ? kQuantStages - 1 : stage - 1;
+    if (pre.g < ts.G) fetch_tile(x + pre.g * matrix, ts.R, ts.C, pre.rb * 128ll, pre.cb * 128ll, ring[ahead]);
+    cp_async_commit();
+    advance(pre, ts, d);
+    body(ring[stage], static_cast<int64_t>(cur.g), cur.rb * 128ll, cur.cb * 128ll);
+    advance(cur, ts, d);
+    stage = stage + 1 == kQuantStages ? 0 : stage + 1;
+  }
+  cp_async_wait<0>();
 }
 
 // Thread (warp w, lane l) of the colwise path owns the 8x8 micro-tile at tile
@@ -164,19 +305,44 @@ __device__ __forceinline__ void read_microtile(const StagedTile& t, uint4 (&v)[8
   for (int i = 0; i < 8; ++i) v[i] = t.chunk[rg * 8 + i][cg ^ rg];  // swz(8 rg + i, cg)
 }
 
-// Packs column j of the micro-tile (8 consecutive rows, already scaled) into
-// 8 e4m3 bytes and stores them at qT[col][row .. row + 8): the 16 lanes of a
-// half-warp cover 128 contiguous bytes of one qT row.
-__device__ __forceinline__ void store_column8(uint8_t* qT, int64_t R, int64_t col, int64_t row, const float (&qv)[8]) {
-  uint2 o;
-  o.x = cvt_e4m3x2(qv[0], qv[1]) | (cvt_e4m3x2(qv[2], qv[3]) << 16);
-  o.y = cvt_e4m3x2(qv[4], qv[5]) | (cvt_e4m3x2(qv[6], qv[7]) << 16);
-  st_v2(qT + col * R + row, o);
+// Column j of the micro-tile (8 consecutive rows) as 8 e4m3 codes of
+// fl32(x / s), or of x * m for MX.
+__device__ __forceinline__ uint2 column8_div(const uint4 (&v)[8], int j, float s, float ny) {
+  const float2 S = make_float2(s, s), NY = make_float2(ny, ny);
+  const float2 a = neg_div_by_scale2(make_float2(elem8(v[0], j), elem8(v[1], j)), S, NY);
+  const float2 b = neg_div_by_scale2(make_float2(elem8(v[2], j), elem8(v[3], j)), S, NY);
+  const float2 c = neg_div_by_scale2(make_float2(elem8(v[4], j), elem8(v[5], j)), S, NY);
+  const float2 d = neg_div_by_scale2(make_float2(elem8(v[6], j), elem8(v[7], j)), S, NY);
+  return make_uint2(e4m3x4_from_neg(a, b), e4m3x4_from_neg(c, d));
 }
 
-// Colwise quantization of the staged tile: a column block spans the 16 lanes
-// of a half-warp (blockwise, 128 rows) or 4 of them (MX, 32 rows); its max is
-// reduced with shuffles inside that group.
+__device__ __forceinline__ uint2 column8_mul(const uint4 (&v)[8], int j, float m) {
+  const float2 M = make_float2(m, m);
+  const float2 a = __fmul2_rn(make_float2(elem8(v[0], j), elem8(v[1], j)), M);
+  const float2 b = __fmul2_rn(make_float2(elem8(v[2], j), elem8(v[3], j)), M);
+  const float2 c = __fmul2_rn(make_float2(elem8(v[4], j), elem8(v[5], j)), M);
+  const float2 d = __fmul2_rn(make_float2(elem8(v[6], j), elem8(v[7], j)), M);
+  return make_uint2(__byte_perm(cvt_e4m3x2(a.x, a.y), cvt_e4m3x2(b.x, b.y), 0x5410),
+                    __byte_perm(cvt_e4m3x2(c.x, c.y), cvt_e4m3x2(d.x, d.y), 0x5410));
+}
+
+// Packed |x| maxes of the micro-tile's column pairs (2k, 2k + 1) over its
+// 8 rows.
+__device__ __forceinline__ void column_pair_maxes(const uint4 (&v)[8], uint32_t (&m)[4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    m[k] = word(v[0], k);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m[k] = absmax_bf16x2(m[k], word(v[i], k));
+  }
+}
+
+// Colwise quantization of the staged tile.  A column block spans the 16
+// lanes of a half-warp (blockwise, 128 rows) or 4 of them (MX, 32 rows); its
+// max is reduced with shuffles inside that group, two columns per packed
+// word.  Each column of the micro-tile is stored as 8 bytes at
+// qT[col][row .. row + 8): the 16 lanes of a half-warp cover 128 contiguous
+// bytes of one qT row.
 template <bool kMX>
 __device__ __forceinline__ void colwise_from_tile(const StagedTile& t, int64_t R, int64_t C, int64_t r0, int64_t c0,
                                                   uint8_t* __restrict__ qT, float* __restrict__ s,
@@ -185,153 +351,133 @@ __device__ __forceinline__ void colwise_from_tile(const StagedTile& t, int64_t R
   const int rg = lane & 15;
   const int64_t row = r0 + rg * 8;
   const int64_t col = c0 + (warp * 2 + (lane >> 4)) * 8;
-  const bool ok = row < R && col < C;  // R % 32 == 0: a 32-row MX block is all in or all out
 
   uint4 v[8];
   read_microtile(t, v);
-  float amax[8];
+  uint32_t m[4];
+  column_pair_maxes(v, m);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float a = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(elem8(v[i], j)));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+  for (int k = 0; k < 4; ++k) {
+    m[k] = shfl_absmax(m[k], 1);
+    m[k] = shfl_absmax(m[k], 2);
     if (!kMX) {
-      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
+      m[k] = shfl_absmax(m[k], 4);
+      m[k] = shfl_absmax(m[k], 8);
     }
-    amax[j] = a;
   }
-  if (!ok) return;
-
+  if (kMX) {
+    if (!(row < R && col < C)) return;  // R % 32 == 0: a 32-row MX block is all in or all out
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float qv[8];
-    if (kMX) {
-      const int E = mx_exponent(amax[j], mode);
-      const float m = pow2_neg(E);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) qv[i] = elem8(v[i], j) * m;
+    for (int j = 0; j < 8; ++j) {
+      const int E = mx_exponent(unpack_amax(m, j), mode);
       if ((rg & 3) == 0) e8[(col + j) * (R / 32) + row / 32] = static_cast<uint8_t>(E + 127);
-    } else {
-      const float sc = blockwise_scale(amax[j]);
-      const float y = __frcp_rn(sc);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) qv[i] = div_by_scale(elem8(v[i], j), sc, y);
-      if (rg == j) s[(r0 / 128) * C + col + j] = sc;
+      st_v2(qT + (col + j) * R + row, column8_mul(v, j, pow2_neg(E)));
     }
-    store_column8(qT, R, col + j, row, qv);
-  }
-}
-
-// Rowwise 1x128 quantization of the 8 row chunks a thread loaded in
-// load_tile (the half-warp of each row holds its 128 columns).  Writes q and
-// leaves each row's scale in s_rows[row of the tile].
-__device__ __forceinline__ void rowwise_from_regs(const uint4 (&v)[8], int64_t C, int64_t r0, int64_t c0,
-                                                  uint8_t* __restrict__ q, float* s_rows) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = lane >> 4, l16 = lane & 15;
+  } else {
+    // Blockwise tiles are whole (R, C multiples of 128).  Lane j of each
+    // half-warp derives column j's scale; shuffles hand it to the others.
+    const float sc = blockwise_scale(unpack_amax(m, rg & 7));
+    const float ny = neg_recip(sc);
+    if (rg < 8) s[(r0 / 128) * C + col + rg] = sc;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float a = amax8(v[i]);
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    const float sc = blockwise_scale(a);
-    const int rl = warp * 16 + i * 2 + h;
-    st_v2(q + (r0 + rl) * C + c0 + l16 * 8, quant8_div(v[i], sc, __frcp_rn(sc)));
-    if (l16 == 0) s_rows[rl] = sc;
+    for (int j = 0; j < 8; ++j) {
+      const float sj = __shfl_sync(0xffffffffu, sc, (lane & 16) | j);
+      const float nyj = __shfl_sync(0xffffffffu, ny, (lane & 16) | j);
+      st_v2(qT + (col + j) * R + row, column8_div(v, j, sj, nyj));
+    }
   }
 }
 
-__global__ void __launch_bounds__(256) quant_1x128_col_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C,
-                                                              uint8_t* __restrict__ qT, float* __restrict__ s) {
-  __shared__ StagedTile tile;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128, c0 = static_cast<int64_t>(blockIdx.x) * 128;
+// Rowwise 1x128 quantization of the staged tile's rows.
+__device__ __forceinline__ void rowwise_from_tile(const StagedTile& t, int64_t R, int64_t C, int64_t r0, int64_t c0,
+                                                  uint8_t* __restrict__ q, float* __restrict__ s) {
   uint4 v[8];
-  load_tile(x, R, C, r0, c0, tile, v);
-  __syncthreads();
-  colwise_from_tile<false>(tile, R, C, r0, c0, qT, s, nullptr, 0);
+  read_rows(t, v);
+  rowwise_quant(v, R, C, r0, c0, q, s);
 }
 
-// Both 1x128 quantizations of one tile from a single read of x: rowwise from
-// the loaded registers, colwise from the staged tile.
-__global__ void __launch_bounds__(256) quant_1x128_rowcol_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C,
-                                                                 uint8_t* __restrict__ q, float* __restrict__ s,
-                                                                 uint8_t* __restrict__ qT, float* __restrict__ sT) {
-  __shared__ StagedTile tile;
-  __shared__ float s_rows[128];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128, c0 = static_cast<int64_t>(blockIdx.x) * 128;
-  uint4 v[8];
-  load_tile(x, R, C, r0, c0, tile, v);
-  rowwise_from_regs(v, C, r0, c0, q, s_rows);
-  __syncthreads();
-  if (threadIdx.x < 128) s[static_cast<int64_t>(blockIdx.x) * R + r0 + threadIdx.x] = s_rows[threadIdx.x];
-  colwise_from_tile<false>(tile, R, C, r0, c0, qT, sT, nullptr, 0);
+__device__ __forceinline__ TileSpace tile_space(int64_t G, int64_t R, int64_t C) {
+  return TileSpace{R, C, static_cast<int>((C + 127) / 128), static_cast<int>((R + 127) / 128), static_cast<int>(G)};
 }
 
-// grid.z = expert index for the 3D case (per-expert strides passed in).
-__global__ void __launch_bounds__(256) mx_quant_col_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C,
-                                                           uint8_t* __restrict__ qT, uint8_t* __restrict__ e8,
-                                                           int mode) {
-  __shared__ StagedTile tile;
-  const int64_t g = blockIdx.z;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128, c0 = static_cast<int64_t>(blockIdx.x) * 128;
-  uint4 v[8];
-  load_tile(x + g * R * C, R, C, r0, c0, tile, v);
-  __syncthreads();
-  colwise_from_tile<true>(tile, R, C, r0, c0, qT + g * R * C, nullptr, e8 + g * C * (R / 32), mode);
+__global__ void __launch_bounds__(256, kQuantCtasPerSm)
+    quant_1x128_col_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, uint8_t* __restrict__ qT,
+                           float* __restrict__ s) {
+  extern __shared__ __align__(128) uint8_t quant_smem[];
+  StagedTile* ring = reinterpret_cast<StagedTile*>(quant_smem);
+  for_each_staged_tile(x, tile_space(1, R, C), ring, [&](const StagedTile& t, int64_t, int64_t r0, int64_t c0) {
+    colwise_from_tile<false>(t, R, C, r0, c0, qT, s, nullptr, 0);
+  });
+}
+
+// Both 1x128 quantizations of one tile from a single read of x.
+__global__ void __launch_bounds__(256, kQuantCtasPerSm)
+    quant_1x128_rowcol_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, uint8_t* __restrict__ q,
+                              float* __restrict__ s, uint8_t* __restrict__ qT, float* __restrict__ sT) {
+  extern __shared__ __align__(128) uint8_t quant_smem[];
+  StagedTile* ring = reinterpret_cast<StagedTile*>(quant_smem);
+  for_each_staged_tile(x, tile_space(1, R, C), ring, [&](const StagedTile& t, int64_t, int64_t r0, int64_t c0) {
+    rowwise_from_tile(t, R, C, r0, c0, q, s);
+    colwise_from_tile<false>(t, R, C, r0, c0, qT, sT, nullptr, 0);
+  });
+}
+
+// G stacked matrices (the 3D expert case; G = 1 for a plain 2D operand).
+__global__ void __launch_bounds__(256, kQuantCtasPerSm)
+    mx_quant_col_kernel(const uint16_t* __restrict__ x, int64_t G, int64_t R, int64_t C, uint8_t* __restrict__ qT,
+                        uint8_t* __restrict__ e8, int mode) {
+  extern __shared__ __align__(128) uint8_t quant_smem[];
+  StagedTile* ring = reinterpret_cast<StagedTile*>(quant_smem);
+  for_each_staged_tile(x, tile_space(G, R, C), ring, [&](const StagedTile& t, int64_t g, int64_t r0, int64_t c0) {
+    colwise_from_tile<true>(t, R, C, r0, c0, qT + g * R * C, nullptr, e8 + g * C * (R / 32), mode);
+  });
 }
 
 // ---------------------------------------------------------------- 128x128
 
-// One scale for the whole tile: the max of the loaded registers reduced over
-// the CTA; q is written row-major from registers (a half-warp per 128-byte row
-// segment), qT from the staged tile's micro-tiles.
-__global__ void __launch_bounds__(256) quant_128x128_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C,
-                                                            uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
-                                                            float* __restrict__ s, int64_t s_ld) {
-  __shared__ StagedTile tile;
+// One scale for the whole tile: the max of the rows reduced over the CTA; q
+// is written row-major (a half-warp per 128-byte row segment), qT from the
+// micro-tiles.
+__global__ void __launch_bounds__(256, kQuantCtasPerSm)
+    quant_128x128_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, uint8_t* __restrict__ q,
+                         uint8_t* __restrict__ qT, float* __restrict__ s, int64_t s_ld) {
+  extern __shared__ __align__(128) uint8_t quant_smem[];
+  StagedTile* ring = reinterpret_cast<StagedTile*>(quant_smem);
   __shared__ float warp_max[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128, c0 = static_cast<int64_t>(blockIdx.x) * 128;
-  uint4 v[8];
-  load_tile(x, R, C, r0, c0, tile, v);
-  float a = 0.0f;
+  for_each_staged_tile(x, tile_space(1, R, C), ring, [&](const StagedTile& t, int64_t, int64_t r0, int64_t c0) {
+    uint4 v[8];
+    read_rows(t, v);
+    uint32_t m = absmax8(v[0]);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) a = fmaxf(a, amax8(v[i]));
+    for (int i = 1; i < 8; ++i) m = absmax_bf16x2(m, absmax8(v[i]));
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-  if (lane == 0) warp_max[warp] = a;
-  __syncthreads();  // also publishes the staged tile
-  a = warp_max[0];
+    for (int o = 16; o > 0; o >>= 1) m = shfl_absmax(m, o);
+    // warp_max is rewritten only after the next tile's leading barrier, which
+    // every thread reaches after its reads below.
+    if (lane == 0) warp_max[warp] = fmaxf(__uint_as_float((m & 0x7FFFu) << 16), __uint_as_float(m & 0x7FFF0000u));
+    __syncthreads();
+    float a = warp_max[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) a = fmaxf(a, warp_max[w]);
-  const float sc = blockwise_scale(a);
-  const float y = __frcp_rn(sc);
-  if (threadIdx.x == 0) s[blockIdx.y * s_ld + blockIdx.x] = sc;
+    for (int w = 1; w < 8; ++w) a = fmaxf(a, warp_max[w]);
+    const float sc = blockwise_scale(a);
+    const float ny = neg_recip(sc);
+    if (threadIdx.x == 0) s[(r0 / 128) * s_ld + c0 / 128] = sc;
 
-  const int h = lane >> 4, l16 = lane & 15;
+    const int h = lane >> 4, l16 = lane & 15;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int64_t r = r0 + warp * 16 + i * 2 + h;
-    st_v2(q + r * C + c0 + l16 * 8, quant8_div(v[i], sc, y));
-  }
-  if (qT != nullptr) {
-    const int rg = lane & 15;
-    const int64_t row = r0 + rg * 8;
-    const int64_t col = c0 + (warp * 2 + (lane >> 4)) * 8;
-    read_microtile(tile, v);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float qv[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) qv[i] = div_by_scale(elem8(v[i], j), sc, y);
-      store_column8(qT, R, col + j, row, qv);
+    for (int i = 0; i < 8; ++i) {
+      const int64_t r = r0 + warp * 16 + i * 2 + h;
+      st_v2(q + r * C + c0 + l16 * 8, quant8_div(v[i], sc, ny));
     }
-  }
+    if (qT != nullptr) {
+      const int64_t row = r0 + (lane & 15) * 8;
+      const int64_t col = c0 + (warp * 2 + (lane >> 4)) * 8;
+      read_microtile(t, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) st_v2(qT + (col + j) * R + row, column8_div(v, j, sc, ny));
+    }
+  });
 }
 
 // ---------------------------------------------------------------- MX 1x32 rowwise
@@ -354,9 +500,8 @@ __global__ void __launch_bounds__(256) mx_quant_row_kernel(const uint16_t* __res
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int64_t r = rbase + i;
-    float a = amax8(v[i]);
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    uint32_t mm = shfl_absmax(shfl_absmax(absmax8(v[i]), 1), 2);
+    const float a = fmaxf(__uint_as_float((mm & 0x7FFFu) << 16), __uint_as_float(mm & 0x7FFF0000u));
     if (!col_ok || r >= R) continue;
     const int E = mx_exponent(a, mode);
     st_v2(q + r * C + col, quant8_mul(v[i], pow2_neg(E)));
@@ -368,6 +513,35 @@ __global__ void __launch_bounds__(256) mx_quant_row_kernel(const uint16_t* __res
 
 static inline cudaError_t finish() { return cudaGetLastError(); }
 
+// Per device, once: the staged-tile kernels' dynamic shared memory limit and
+// the SM count that sizes their persistent grids.
+static int staged_grid_cap() {
+  static std::mutex mu;
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+    const int smem = static_cast<int>(kQuantSmem);
+    if (cudaFuncSetAttribute(quant_1x128_col_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ||
+        cudaFuncSetAttribute(quant_1x128_rowcol_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ||
+        cudaFuncSetAttribute(mx_quant_col_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ||
+        cudaFuncSetAttribute(quant_128x128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))
+      return 0;
+    sms[dev] = n;
+  }
+  return sms[dev] * kQuantCtasPerSm;
+}
+
+static inline bool staged_grid(int64_t tiles, dim3& grid) {
+  const int cap = staged_grid_cap();
+  if (cap <= 0) return false;
+  grid = dim3(static_cast<unsigned>(tiles < cap ? tiles : cap));
+  return true;
+}
+
 cudaError_t launch_quant_1x128_row(const uint16_t* x, int64_t R, int64_t C, uint8_t* q, float* s, cudaStream_t st) {
   dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(R / 128));
   quant_1x128_row_kernel<<<grid, 256, 0, st>>>(x, R, C, q, s);
@@ -375,22 +549,25 @@ cudaError_t launch_quant_1x128_row(const uint16_t* x, int64_t R, int64_t C, uint
 }
 
 cudaError_t launch_quant_1x128_col(const uint16_t* x, int64_t R, int64_t C, uint8_t* qT, float* s, cudaStream_t st) {
-  dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(R / 128));
-  quant_1x128_col_kernel<<<grid, 256, 0, st>>>(x, R, C, qT, s);
+  dim3 grid;
+  if (!staged_grid((R / 128) * (C / 128), grid)) return cudaErrorInvalidConfiguration;
+  quant_1x128_col_kernel<<<grid, 256, kQuantSmem, st>>>(x, R, C, qT, s);
   return finish();
 }
 
 cudaError_t launch_quant_1x128_rowcol(const uint16_t* x, int64_t R, int64_t C, uint8_t* q, float* s, uint8_t* qT,
                                       float* sT, cudaStream_t st) {
-  dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(R / 128));
-  quant_1x128_rowcol_kernel<<<grid, 256, 0, st>>>(x, R, C, q, s, qT, sT);
+  dim3 grid;
+  if (!staged_grid((R / 128) * (C / 128), grid)) return cudaErrorInvalidConfiguration;
+  quant_1x128_rowcol_kernel<<<grid, 256, kQuantSmem, st>>>(x, R, C, q, s, qT, sT);
   return finish();
 }
 
 cudaError_t launch_quant_128x128(const uint16_t* w, int64_t R, int64_t C, uint8_t* q, uint8_t* qT, float* s,
                                  int64_t s_ld, cudaStream_t st) {
-  dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(R / 128));
-  quant_128x128_kernel<<<grid, 256, 0, st>>>(w, R, C, q, qT, s, s_ld);
+  dim3 grid;
+  if (!staged_grid((R / 128) * (C / 128), grid)) return cudaErrorInvalidConfiguration;
+  quant_128x128_kernel<<<grid, 256, kQuantSmem, st>>>(w, R, C, q, qT, s, s_ld);
   return finish();
 }
 
@@ -403,8 +580,9 @@ cudaError_t launch_mx_quant_row(const uint16_t* x, int64_t R, int64_t C, uint8_t
 
 cudaError_t launch_mx_quant_col(const uint16_t* x, int64_t G, int64_t R, int64_t C, uint8_t* qT, uint8_t* e8,
                                 int mode, cudaStream_t st) {
-  dim3 grid(static_cast<unsigned>((C + 127) / 128), static_cast<unsigned>((R + 127) / 128), static_cast<unsigned>(G));
-  mx_quant_col_kernel<<<grid, 256, 0, st>>>(x, R, C, qT, e8, mode);
+  dim3 grid;
+  if (!staged_grid(G * ((R + 127) / 128) * ((C + 127) / 128), grid)) return cudaErrorInvalidConfiguration;
+  mx_quant_col_kernel<<<grid, 256, kQuantSmem, st>>>(x, G, R, C, qT, e8, mode);
   return finish();
 }
 
