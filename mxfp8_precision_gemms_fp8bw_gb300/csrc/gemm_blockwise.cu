@@ -24,7 +24,11 @@
 //               warps 4-7 columns 0-127 and warps 8-11 columns 128-255 of the
 //               partial, multiply-add it into 128 fp32 accumulators per
 //               thread, release the buffer, and after the last block write
-//               their row of the bf16 output tile.
+//               their part of the bf16 output tile.  With one B scale per
+//               128x128 block (fwd, dgrad) a thread owns one row (32x32b
+//               TMEM loads); with one B scale per column (wgrad) a thread
+//               owns 4 rows x 32 columns (16x256b loads), which divides the
+//               broadcast reads of the column scales by four.
 // The MMA of block kb+1 runs while block kb is being promoted.
 //
 // Every wait is bounded (see mbar_wait): a lost arrival makes the kernel
@@ -86,6 +90,109 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
 
 __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Promotion with a per-column B scale (wgrad: both operands in 1x128 blocks
+// along the contraction), out[i, j] = sum_kb sa[kb][i] * sb[kb][j] * P_kb[i, j].
+// Every column of a block has its own scale, which every row needs.  Reading
+// the partial with the 16x256b TMEM shape gives each thread 4 rows x 32
+// columns (two adjacent columns of every 8), so one broadcast 8-byte shared
+// load per 8-column chunk and lane half serves two rows: a quarter of the
+// shared-memory wavefronts that one row per thread costs, where the
+// broadcasts would otherwise saturate the shared-memory pipe.
+__device__ __forceinline__ void promote_per_column(SharedStorage& sm, uint32_t tmem, int ew, int half, int quarter,
+                                                   int lane, int num_tiles, int num_m, int num_n, int num_k,
+                                                   const float* __restrict__ sa, int64_t sa_ld,
+                                                   const float* __restrict__ sb, int64_t sb_ld_kb,
+                                                   uint16_t* __restrict__ out, int No, int* status, AbortFlag ab) {
+  const int q4 = lane & 3, r8 = lane >> 2;
+  int buf = 0;
+  uint32_t tphase = 0;
+  bool alive = true;
+  for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
+    int mb, nb;
+    tile_coords(tile, num_m, num_n, mb, nb);
+    const int64_t rbase = static_cast<int64_t>(mb) * BM + quarter * 32 + r8;  // rows rbase + 16h + 8e
+    const int64_t col0 = static_cast<int64_t>(nb) * BN + half * 128;
+    float2 acc[64];  // column pair 2*q4 of chunk k, row 16h + 8e: acc[(h * 16 + k) * 2 + e]
+#pragma unroll
+    for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
+
+    // Scales of the next block are fetched one block ahead; each lane fetches
+    // four consecutive column scales of the warp's 128 (one coalesced 512-byte
+    // row per warp) and stages them in the warp's own shared buffer.
+    float sa_next[4];  // [h * 2 + e]
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sa_next[i] = __ldg(sa + rbase + 16 * (i >> 1) + 8 * (i & 1));
+    float4 sb4_next = __ldg(reinterpret_cast<const float4*>(sb + col0) + lane);
+    for (int kb = 0; kb < num_k; ++kb) {
+      float sa_cur[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sa_cur[i] = sa_next[i];
+      // The buffer written now was last read two blocks ago; every lane
+      // finished those reads before the previous block's __syncwarp.
+      reinterpret_cast<float4*>(sm.sb_vec[ew][kb & 1])[lane] = sb4_next;
+      __syncwarp();
+      if (kb + 1 < num_k) {
+        const float* sak = sa + static_cast<int64_t>(kb + 1) * sa_ld;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sa_next[i] = __ldg(sak + rbase + 16 * (i >> 1) + 8 * (i & 1));
+        sb4_next = __ldg(reinterpret_cast<const float4*>(sb + static_cast<int64_t>(kb + 1) * sb_ld_kb + col0) + lane);
+      }
+      if (!mbar_wait(&sm.tmem_full[buf], tphase, ab, status)) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t t_col = tmem + static_cast<uint32_t>(buf * BN + half * 128);
+      const float* sbv = sm.sb_vec[ew][kb & 1];
+      // Eight load/wait rounds of 16 lanes x 32 columns: column quarter cq
+      // of the warp's 128 columns, lane half h of its 32 TMEM lanes.
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const int cq = g >> 1, h = g & 1;
+        uint32_t r[16];
+        tmem_ld_16x256b_x4(t_col + (static_cast<uint32_t>(quarter * 32 + 16 * h) << 16) + cq * 32, r);
+        tmem_ld_wait();
+        if (g == 7) {
+          // The whole partial is in registers: the buffer goes back to the MMA warp.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
+        }
+        const float2 fa0 = make_float2(sa_cur[h * 2], sa_cur[h * 2]);
+        const float2 fa1 = make_float2(sa_cur[h * 2 + 1], sa_cur[h * 2 + 1]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int k = cq * 4 + c;
+          const float2 s2 = *reinterpret_cast<const float2*>(sbv + 8 * k + 2 * q4);
+          const float2 p0 = make_float2(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]));
+          const float2 p1 = make_float2(__uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
+          float2& a0 = acc[(h * 16 + k) * 2];
+          float2& a1 = acc[(h * 16 + k) * 2 + 1];
+          a0 = __ffma2_rn(__fmul2_rn(p0, s2), fa0, a0);
+          a1 = __ffma2_rn(__fmul2_rn(p1, s2), fa1, a1);
+        }
+      }
+      if (++buf == 2) {
+        buf = 0;
+        tphase ^= 1u;
+      }
+    }
+    if (!alive) break;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        uint32_t* orow = reinterpret_cast<uint32_t*>(out + (rbase + 16 * h + 8 * e) * No + col0 + 2 * q4);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float2 v = acc[(h * 16 + k) * 2 + e];
+          orow[4 * k] = pack_bf16x2(v.x, v.y);
+        }
+      }
+    }
+  }
 }
 
 template <int kBScale>
@@ -220,101 +327,84 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int ew = warp - EPI_WARP0;
     const int half = ew >> 2;                  // column half of the tile
     const int quarter = warp & 3;              // TMEM lane quarter this warp may access
-    const int row = quarter * 32 + lane;       // row of the tile this thread owns
-    const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
-    int buf = 0;
-    uint32_t tphase = 0;
-    bool alive = true;
-    for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
-      int mb, nb;
-      tile_coords(tile, num_m, num_n, mb, nb);
-      const int64_t m = static_cast<int64_t>(mb) * BM + row;
-      const int64_t col0 = static_cast<int64_t>(nb) * BN + half * 128;
-      float2 acc[64];
+    if constexpr (kBScale == 1) {
+      promote_per_column(sm, tmem, ew, half, quarter, lane, num_tiles, num_m, num_n, num_k, sa, sa_ld, sb, sb_ld_kb,
+                         out, No, status, ab);
+    } else {
+      const int row = quarter * 32 + lane;       // row of the tile this thread owns
+      const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+      int buf = 0;
+      uint32_t tphase = 0;
+      bool alive = true;
+      for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, num_m, num_n, mb, nb);
+        const int64_t m = static_cast<int64_t>(mb) * BM + row;
+        const int64_t col0 = static_cast<int64_t>(nb) * BN + half * 128;
+        float2 acc[64];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
+        for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
 
-      // Scales of the next block are fetched one block ahead.  Per-block B
-      // scale: one value per thread.  Per-column B scale: each lane fetches
-      // four consecutive columns of the warp's 128 (one coalesced 512-byte
-      // row per warp) and stages them in the warp's own shared buffer.
-      float sa_next = __ldg(sa + m);
-      float sb_next = kBScale == 0 ? __ldg(sb + (col0 / 128) * sb_ld_nb) : 0.0f;
-      float4 sb4_next = kBScale == 1 ? __ldg(reinterpret_cast<const float4*>(sb + col0) + lane)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int kb = 0; kb < num_k; ++kb) {
-        const float sa_cur = sa_next;
-        const float sb_cur = sb_next;
-        if (kBScale == 1) {
-          // The buffer written now was last read two blocks ago; every lane
-          // finished those reads before the previous block's __syncwarp.
-          reinterpret_cast<float4*>(sm.sb_vec[ew][kb & 1])[lane] = sb4_next;
-          __syncwarp();
-        }
-        if (kb + 1 < num_k) {
-          sa_next = __ldg(sa + static_cast<int64_t>(kb + 1) * sa_ld + m);
-          if (kBScale == 0)
+        // Scales of the next block are fetched one block ahead: the row's A
+        // scale and the tile half's B block scale.
+        float sa_next = __ldg(sa + m);
+        float sb_next = __ldg(sb + (col0 / 128) * sb_ld_nb);
+        for (int kb = 0; kb < num_k; ++kb) {
+          const float sa_cur = sa_next;
+          const float sb_cur = sb_next;
+          if (kb + 1 < num_k) {
+            sa_next = __ldg(sa + static_cast<int64_t>(kb + 1) * sa_ld + m);
             sb_next = __ldg(sb + (col0 / 128) * sb_ld_nb + static_cast<int64_t>(kb + 1) * sb_ld_kb);
-          else
-            sb4_next = __ldg(reinterpret_cast<const float4*>(sb + static_cast<int64_t>(kb + 1) * sb_ld_kb + col0) + lane);
-        }
-        if (!mbar_wait(&sm.tmem_full[buf], tphase, ab, status)) {
-          alive = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t t_base = tmem + t_lane + static_cast<uint32_t>(buf * BN + half * 128);
-        // 16-column TMEM loads, NC of them in flight per wait: one for the
-        // per-block B scale (eight load/wait rounds per block measured fastest),
-        // four for the per-column B scale (two rounds).  The buffer goes back
-        // to the MMA warp as soon as the last load has landed in registers.
-        constexpr int NC = kBScale == 0 ? 1 : 4;
-        constexpr int NG = 8 / NC;
-        const float2 fa = make_float2(sa_cur, sa_cur);
-        const float2 f2 = kBScale == 0 ? make_float2(sa_cur * sb_cur, sa_cur * sb_cur) : fa;
-        const float* sbv = sm.sb_vec[ew][kb & 1];
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          uint32_t r[NC][16];
-#pragma unroll
-          for (int c = 0; c < NC; ++c) tmem_ld_32x32b_x16(t_base + (g * NC + c) * 16, r[c]);
-          tmem_ld_wait();
-          if (g == NG - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
           }
+          if (!mbar_wait(&sm.tmem_full[buf], tphase, ab, status)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t t_base = tmem + t_lane + static_cast<uint32_t>(buf * BN + half * 128);
+          // 16-column TMEM loads, one per wait (eight load/wait rounds per
+          // block measured fastest).  The buffer goes back to the MMA warp as
+          // soon as the last load has landed in registers.
+          constexpr int NC = 1;
+          constexpr int NG = 8 / NC;
+          const float2 f2 = make_float2(sa_cur * sb_cur, sa_cur * sb_cur);
 #pragma unroll
-          for (int c = 0; c < NC; ++c) {
-            const int col = (g * NC + c) * 16;
+          for (int g = 0; g < NG; ++g) {
+            uint32_t r[NC][16];
 #pragma unroll
-            for (int j = 0; j < 8; j += 2) {
-              const float2 p0 = make_float2(__uint_as_float(r[c][2 * j]), __uint_as_float(r[c][2 * j + 1]));
-              const float2 p1 = make_float2(__uint_as_float(r[c][2 * j + 2]), __uint_as_float(r[c][2 * j + 3]));
-              float2& a0 = acc[(col >> 1) + j];
-              float2& a1 = acc[(col >> 1) + j + 1];
-              if (kBScale == 0) {
+            for (int c = 0; c < NC; ++c) tmem_ld_32x32b_x16(t_base + (g * NC + c) * 16, r[c]);
+            tmem_ld_wait();
+            if (g == NG - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
+            }
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+              const int col = (g * NC + c) * 16;
+#pragma unroll
+              for (int j = 0; j < 8; j += 2) {
+                const float2 p0 = make_float2(__uint_as_float(r[c][2 * j]), __uint_as_float(r[c][2 * j + 1]));
+                const float2 p1 = make_float2(__uint_as_float(r[c][2 * j + 2]), __uint_as_float(r[c][2 * j + 3]));
+                float2& a0 = acc[(col >> 1) + j];
+                float2& a1 = acc[(col >> 1) + j + 1];
                 a0 = __ffma2_rn(p0, f2, a0);
                 a1 = __ffma2_rn(p1, f2, a1);
-              } else {
-                const float4 s4 = *reinterpret_cast<const float4*>(sbv + col + 2 * j);
-                a0 = __ffma2_rn(__fmul2_rn(p0, make_float2(s4.x, s4.y)), fa, a0);
-                a1 = __ffma2_rn(__fmul2_rn(p1, make_float2(s4.z, s4.w)), fa, a1);
               }
             }
           }
+          if (++buf == 2) {
+            buf = 0;
+            tphase ^= 1u;
+          }
         }
-        if (++buf == 2) {
-          buf = 0;
-          tphase ^= 1u;
-        }
-      }
-      if (!alive) break;
-      uint16_t* orow = out + m * No + col0;
+        if (!alive) break;
+        uint16_t* orow = out + m * No + col0;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        st_global_v4(orow + c * 8, pack_bf16x2(acc[4 * c].x, acc[4 * c].y), pack_bf16x2(acc[4 * c + 1].x, acc[4 * c + 1].y),
-                     pack_bf16x2(acc[4 * c + 2].x, acc[4 * c + 2].y), pack_bf16x2(acc[4 * c + 3].x, acc[4 * c + 3].y));
+        for (int c = 0; c < 16; ++c) {
+          st_global_v4(orow + c * 8, pack_bf16x2(acc[4 * c].x, acc[4 * c].y), pack_bf16x2(acc[4 * c + 1].x, acc[4 * c + 1].y),
+                       pack_bf16x2(acc[4 * c + 2].x, acc[4 * c + 2].y), pack_bf16x2(acc[4 * c + 3].x, acc[4 * c + 3].y));
+        }
       }
     }
   }
