@@ -50,6 +50,7 @@ constexpr int EPI_WARP0 = 4;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;  // two BN-column fp32 partial buffers
 constexpr int GROUP_M = 16;          // tile raster: 16 row-blocks share a column sweep
+constexpr int SB_STRIDE = 36;        // floats per lane-quarter row of the staged column scales
 // Register split.  Each SM sub-partition holds one warp of every warpgroup and
 // 16384 registers, so a 384-thread CTA launches with 168 per thread; warpgroup
 // 0 (producer, MMA, TMEM owner) then gives up registers to warpgroups 1-2
@@ -66,7 +67,11 @@ struct RegSplit {
 struct SharedStorage {
   uint8_t a[STAGES][A_BYTES];  // each stage 1024-byte aligned (swizzle atom)
   uint8_t b[STAGES][B_BYTES];
-  float sb_vec[NUM_EPI_WARPS][2][128];  // per-column B scales, private to each promotion warp: [warp][buffer][column]
+  // Per-column B scales of the current and next block, private to each
+  // promotion warp: [warp][buffer][SB_STRIDE * q + 2 * chunk + e] holds column
+  // 8 * chunk + 2 * q + e (q = lane % 4), so a thread's 32 scales are
+  // contiguous and its 16-byte loads of two chunks hit distinct banks.
+  float sb_vec[NUM_EPI_WARPS][2][4 * SB_STRIDE];
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t tmem_full[2];
@@ -88,6 +93,17 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
   nb = t / gm;
 }
 
+// Explicit shared-memory accesses (a generic pointer into the dynamic
+// shared block would compile to generic loads with global-memory latency).
+__device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts_f32x2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+
 __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -96,10 +112,11 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, ui
 // along the contraction), out[i, j] = sum_kb sa[kb][i] * sb[kb][j] * P_kb[i, j].
 // Every column of a block has its own scale, which every row needs.  Reading
 // the partial with the 16x256b TMEM shape gives each thread 4 rows x 32
-// columns (two adjacent columns of every 8), so one broadcast 8-byte shared
-// load per 8-column chunk and lane half serves two rows: a quarter of the
-// shared-memory wavefronts that one row per thread costs, where the
-// broadcasts would otherwise saturate the shared-memory pipe.
+// columns (two adjacent columns of every 8), so it needs 32 of the 128 column
+// scales.  They are staged per warp in a layout where those 32 are
+// contiguous: one conflict-free 16-byte shared load covers two chunks for
+// both lane halves (8 loads per thread per block).  Shared-memory loads
+// compete with the tensor core's operand reads, so they are kept this few.
 __device__ __forceinline__ void promote_per_column(SharedStorage& sm, uint32_t tmem, int ew, int half, int quarter,
                                                    int lane, int num_tiles, int num_m, int num_n, int num_k,
                                                    const float* __restrict__ sa, int64_t sa_ld,
@@ -131,7 +148,13 @@ __device__ __forceinline__ void promote_per_column(SharedStorage& sm, uint32_t t
       for (int i = 0; i < 4; ++i) sa_cur[i] = sa_next[i];
       // The buffer written now was last read two blocks ago; every lane
       // finished those reads before the previous block's __syncwarp.
-      reinterpret_cast<float4*>(sm.sb_vec[ew][kb & 1])[lane] = sb4_next;
+      {
+        // Lane L holds columns 4L .. 4L + 3: chunk L / 2, quarters 2 (L % 2)
+        // and 2 (L % 2) + 1.
+        const uint32_t dst = smem_u32(sm.sb_vec[ew][kb & 1] + (2 * (lane & 1)) * SB_STRIDE + 2 * (lane >> 1));
+        sts_f32x2(dst, sb4_next.x, sb4_next.y);
+        sts_f32x2(dst + SB_STRIDE * 4, sb4_next.z, sb4_next.w);
+      }
       __syncwarp();
       if (kb + 1 < num_k) {
         const float* sak = sa + static_cast<int64_t>(kb + 1) * sa_ld;
@@ -145,33 +168,39 @@ __device__ __forceinline__ void promote_per_column(SharedStorage& sm, uint32_t t
       }
       tc_fence_after();
       const uint32_t t_col = tmem + static_cast<uint32_t>(buf * BN + half * 128);
-      const float* sbv = sm.sb_vec[ew][kb & 1];
+      const uint32_t sbv = smem_u32(sm.sb_vec[ew][kb & 1] + q4 * SB_STRIDE);
       // Eight load/wait rounds of 16 lanes x 32 columns: column quarter cq
-      // of the warp's 128 columns, lane half h of its 32 TMEM lanes.
+      // of the warp's 128 columns, lane half h of its 32 TMEM lanes.  The
+      // scales of a column quarter (chunks 4cq .. 4cq + 3) serve both halves.
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        const int cq = g >> 1, h = g & 1;
-        uint32_t r[16];
-        tmem_ld_16x256b_x4(t_col + (static_cast<uint32_t>(quarter * 32 + 16 * h) << 16) + cq * 32, r);
-        tmem_ld_wait();
-        if (g == 7) {
-          // The whole partial is in registers: the buffer goes back to the MMA warp.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
-        }
-        const float2 fa0 = make_float2(sa_cur[h * 2], sa_cur[h * 2]);
-        const float2 fa1 = make_float2(sa_cur[h * 2 + 1], sa_cur[h * 2 + 1]);
+      for (int cq = 0; cq < 4; ++cq) {
+        const float4 s01 = lds_f32x4(sbv + 32 * cq);       // chunks 4cq, 4cq + 1
+        const float4 s23 = lds_f32x4(sbv + 32 * cq + 16);  // chunks 4cq + 2, 4cq + 3
+        const float2 sc[4] = {make_float2(s01.x, s01.y), make_float2(s01.z, s01.w), make_float2(s23.x, s23.y),
+                              make_float2(s23.z, s23.w)};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int k = cq * 4 + c;
-          const float2 s2 = *reinterpret_cast<const float2*>(sbv + 8 * k + 2 * q4);
-          const float2 p0 = make_float2(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]));
-          const float2 p1 = make_float2(__uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
-          float2& a0 = acc[(h * 16 + k) * 2];
-          float2& a1 = acc[(h * 16 + k) * 2 + 1];
-          a0 = __ffma2_rn(__fmul2_rn(p0, s2), fa0, a0);
-          a1 = __ffma2_rn(__fmul2_rn(p1, s2), fa1, a1);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t r[16];
+          tmem_ld_16x256b_x4(t_col + (static_cast<uint32_t>(quarter * 32 + 16 * h) << 16) + cq * 32, r);
+          tmem_ld_wait();
+          if (cq == 3 && h == 1) {
+            // The whole partial is in registers: the buffer goes back to the MMA warp.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
+          }
+          const float2 fa0 = make_float2(sa_cur[h * 2], sa_cur[h * 2]);
+          const float2 fa1 = make_float2(sa_cur[h * 2 + 1], sa_cur[h * 2 + 1]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int k = cq * 4 + c;
+            const float2 p0 = make_float2(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]));
+            const float2 p1 = make_float2(__uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
+            float2& a0 = acc[(h * 16 + k) * 2];
+            float2& a1 = acc[(h * 16 + k) * 2 + 1];
+            a0 = __ffma2_rn(__fmul2_rn(p0, sc[c]), fa0, a0);
+            a1 = __ffma2_rn(__fmul2_rn(p1, sc[c]), fa1, a1);
+          }
         }
       }
       if (++buf == 2) {
