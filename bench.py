@@ -292,6 +292,8 @@ def run_ours(args, world, rank, local):
 
     moe = None if args.no_moe else run_moe(dev, max(10, args.steps // 3), args.warmup, fp8_peak, peaks["hbm_gbs"],
                                            world)
+    mx_dense = None if args.no_moe else run_moe(dev, max(10, args.steps // 3), args.warmup, fp8_peak,
+                                                peaks["hbm_gbs"], world, dense=True)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -317,10 +319,20 @@ def run_ours(args, world, rank, local):
             "quant_gbs": round(quant_bytes / (quant_ms * 1e-3) / 1e9, 1),
             "hbm_peak_gbs": peaks["hbm_gbs"],
             "kernels": kernels,
+            "linear_us": linear_us(per_kernel, ["quant_1x128_rowcol(x)", "quant_128x128(W)", "gemm_fwd"]),
             "mxfp8_moe": moe,
+            "mxfp8_dense": mx_dense,
         }
         print(json.dumps(line))
     return 0
+
+
+def linear_us(per_kernel, fwd_names):
+    """Per-linear end-to-end times in the microbenchmark columns of PR #3037:
+    forward (its quantizations and GEMM) and forward + backward (the whole
+    step), in microseconds, from the per-launch event times."""
+    return {"fwd_us": round(1e3 * sum(per_kernel[n] for n in fwd_names), 1),
+            "fwd_bwd_us": round(1e3 * sum(per_kernel.values()), 1)}
 
 
 def time_kernels(kern, steps, stream):
@@ -355,16 +367,24 @@ def kernel_table(per, algo, fp8_peak, hbm_peak):
     return out
 
 
-def run_moe(dev, steps, warmup, fp8_peak, hbm_peak, world):
+def run_moe(dev, steps, warmup, fp8_peak, hbm_peak, world, dense: bool = False):
     """The MXFP8 MoE grouped linear step (M=16384 tokens over 8 experts,
-    K=5120, N=8192): nine launches, timed like the dense step."""
+    K=5120, N=8192): nine launches, timed like the dense step.  With
+    dense=True, the MXFP8 dense linear instead: the same nine calls with one
+    group on the dense workload's x, W, dy (M=16384, K=5120, N=8192)."""
     import torch
 
     from mxfp8_precision_gemms_fp8bw_gb300 import binding as B
     from mxfp8_precision_gemms_fp8bw_gb300 import inputs
     from mxfp8_precision_gemms_fp8bw_gb300.linear import MxMoEWorkspace
 
-    t = inputs.moe()
+    if dense:
+        t = dense_inputs()
+        M, K = t.x.shape
+        N = t.w.shape[0]
+        t = inputs.MoEInputs(x=t.x, w=t.w.reshape(1, N, K), dy=t.dy, group_end=np.array([M], np.int32))
+    else:
+        t = inputs.moe()
     G, N, K = t.w.shape
     M = t.x.shape[0]
     x, w, dy = t.x.to(dev), t.w.to(dev), t.dy.to(dev)
@@ -384,15 +404,20 @@ def run_moe(dev, steps, warmup, fp8_peak, hbm_peak, world):
     dom = max(gemm_names, key=lambda n: per[n])
     dom_ach = algo[dom][1] / (per[dom] * 1e-3) / 1e12
     sizes = [int(v) for v in np.diff(np.concatenate([[0], t.group_end]))]
+    workload = (f"MXFP8 dense linear fwd+bwd (one group), M={M} K={K} N={N}, the dense workload's x W dy, "
+                f"1x32 E8M0 RCEIL, seed 2" if dense else
+                f"MXFP8 MoE grouped linear fwd+bwd, M={M} tokens over G={G} experts (sizes {sizes}), "
+                f"K={K}, N={N}, 1x32 E8M0 RCEIL, seed 4")
     return {
-        "workload": f"MXFP8 MoE grouped linear fwd+bwd, M={M} tokens over G={G} experts (sizes {sizes}), "
-                    f"K={K}, N={N}, 1x32 E8M0 RCEIL, seed 4",
+        "workload": workload,
         "value": round(flops * world / (ms_step * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
         "ms_per_step": round(ms_step, 4), "steps": steps, "gpu_launches": len(kern) * steps,
         "gemm_tflops": round(flops / (sum(per[n] for n in gemm_names) * 1e-3) / 1e12, 1),
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(dom_ach, 1), "peak": round(fp8_peak, 1),
-                     "unit": "TFLOP/s", "frac": round(dom_ach / fp8_peak, 4), "traffic": load_traffic(dom)},
+                     "unit": "TFLOP/s", "frac": round(dom_ach / fp8_peak, 4),
+                     "traffic": load_traffic(("mxfp8_dense/" if dense else "") + dom)},
         "kernels": kernel_table(per, algo, fp8_peak, hbm_peak),
+        "linear_us": linear_us(per, ["mx_quant_1x32_row(x)", "mx_quant_1x32_row(W)", "mx_grouped_fwd"]),
     }
 
 
@@ -433,7 +458,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-moe", action="store_true", help="skip the MXFP8 MoE section")
+    ap.add_argument("--no-moe", action="store_true", help="skip the MXFP8 sections (MoE and dense)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     world, rank, local = dist_setup(args.gpus)

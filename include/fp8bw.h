@@ -147,6 +147,18 @@ int fp8bw_gemm_dgrad(const uint8_t* dyq, const float* dys, const uint8_t* wqT, c
 int fp8bw_gemm_wgrad(const uint8_t* dyqT, const float* dysT, const uint8_t* xqT, const float* xsT,
                      fp8bw_bf16* dW, int64_t M, int64_t N, int64_t K, void* stream);
 
+/* dW += dy^T x with dW in fp32: the wgrad GEMM above, its tile added to the
+ * caller's fp32 gradient instead of overwriting a bf16 one -- gradient
+ * accumulation over micro-batches or token shards, whose sum the optimizer
+ * step consumes (PR #4295 "Testing": gradients compared after the expected
+ * reduction, parameters after the optimizer step; PR #2386: grad_weight of
+ * the 128_1_128_1 GEMM).  Arguments as fp8bw_gemm_wgrad; dW : fp32 [N, K],
+ * read and written, 16-byte aligned, owned by the caller.  Each element
+ * receives one fp32 addition of its fp32-promoted tile value.  Calls that
+ * write the same dW must be ordered on one stream. */
+int fp8bw_gemm_wgrad_acc_f32(const uint8_t* dyqT, const float* dysT, const uint8_t* xqT, const float* xsT,
+                             float* dW, int64_t M, int64_t N, int64_t K, void* stream);
+
 /* ---------------------------------------------------------------------------
  * MXFP8: 1x32 blocks, E8M0 scales, e4m3 data ([PR3037] MoEScalingType.MXFP8).
  * ------------------------------------------------------------------------- */

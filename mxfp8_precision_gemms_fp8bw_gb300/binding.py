@@ -34,6 +34,7 @@ _SIGNATURES = {
     "fp8bw_gemm_fwd": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
     "fp8bw_gemm_dgrad": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
     "fp8bw_gemm_wgrad": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
+    "fp8bw_gemm_wgrad_acc_f32": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
     "mxfp8_quant_1x32_row": [_P, _I64, _I64, _P, _P, _INT, _P],
     "mxfp8_quant_1x32_col": [_P, _I64, _I64, _P, _P, _INT, _P],
     "mxfp8_quant_3d_col": [_P, _I64, _I64, _I64, _P, _P, _INT, _P],
@@ -174,6 +175,14 @@ def fp8bw_gemm_wgrad(dyqT, dysT, xqT, xsT, dW, stream=None) -> None:
     K = xqT.shape[0]
     _check(lib().fp8bw_gemm_wgrad(_ptr(dyqT, _U8, "dyqT"), _ptr(dysT, _F32, "dysT"), _ptr(xqT, _U8, "xqT"),
                                   _ptr(xsT, _F32, "xsT"), _ptr(dW, _BF16, "dW"), M, N, K, _stream(stream)))
+
+
+def fp8bw_gemm_wgrad_acc_f32(dyqT, dysT, xqT, xsT, dW, stream=None) -> None:
+    """dW (fp32 [N, K]) += dy^T x."""
+    N, M = dyqT.shape
+    K = xqT.shape[0]
+    _check(lib().fp8bw_gemm_wgrad_acc_f32(_ptr(dyqT, _U8, "dyqT"), _ptr(dysT, _F32, "dysT"), _ptr(xqT, _U8, "xqT"),
+                                          _ptr(xsT, _F32, "xsT"), _ptr(dW, _F32, "dW"), M, N, K, _stream(stream)))
 
 
 def mxfp8_grouped_gemm_workspace_bytes(kind, G, M, N, K) -> int:

@@ -235,16 +235,18 @@ FP8BW_API int mxfp8_quant_3d_col(const fp8bw_bf16* w, int64_t G, int64_t N, int6
 // ============================================================ blockwise GEMMs
 
 static int gemm_common(const char* name, fp8bw::BlockwiseGemmArgs& g, void* stream) {
-  if (!g.a || !g.b || !g.sa || !g.sb || !g.out)
+  void* out = g.out_acc ? static_cast<void*>(g.out_acc) : static_cast<void*>(g.out);
+  const int64_t out_elem = g.out_acc ? 4 : 2;
+  if (!g.a || !g.b || !g.sa || !g.sb || !out)
     return fail(FP8BW_ERR_NULL, "%s: every operand, scale and output pointer must be non-NULL", name);
   if (!dim_ok(g.Mo, 128) || !dim_ok(g.No, 256) || !dim_ok(g.Kc, 128))
     return fail(FP8BW_ERR_SHAPE,
                 "%s: output rows (%lld) and the contraction (%lld) must be positive multiples of 128, output columns "
                 "(%lld) of 256",
                 name, (long long)g.Mo, (long long)g.Kc, (long long)g.No);
-  if (!aligned16(g.a) || !aligned16(g.b) || !aligned16(g.sa) || !aligned16(g.sb) || !aligned16(g.out))
+  if (!aligned16(g.a) || !aligned16(g.b) || !aligned16(g.sa) || !aligned16(g.sb) || !aligned16(out))
     return fail(FP8BW_ERR_ALIGN, "%s: pointers must be 16-byte aligned", name);
-  if (overlaps(g.out, g.Mo * g.No * 2, g.a, g.Mo * g.Kc) || overlaps(g.out, g.Mo * g.No * 2, g.b, g.No * g.Kc))
+  if (overlaps(out, g.Mo * g.No * out_elem, g.a, g.Mo * g.Kc) || overlaps(out, g.Mo * g.No * out_elem, g.b, g.No * g.Kc))
     return fail(FP8BW_ERR_LAYOUT, "%s: the output overlaps an operand", name);
   DeviceState* d;
   if (int rc = current_device(&d)) return rc;
@@ -306,6 +308,25 @@ FP8BW_API int fp8bw_gemm_wgrad(const uint8_t* dyqT, const float* dysT, const uin
   g.No = K;
   g.Kc = M;
   return gemm_common("fp8bw_gemm_wgrad", g, stream);
+}
+
+FP8BW_API int fp8bw_gemm_wgrad_acc_f32(const uint8_t* dyqT, const float* dysT, const uint8_t* xqT, const float* xsT,
+                                       float* dW, int64_t M, int64_t N, int64_t K, void* stream) {
+  fp8bw::BlockwiseGemmArgs g{};
+  g.a = dyqT;
+  g.b = xqT;
+  g.sa = dysT;
+  g.sa_ld = N;
+  g.sb = xsT;
+  g.sb_ld_nb = 0;
+  g.sb_ld_kb = K;
+  g.b_scale = fp8bw::BScale::kPerRow;
+  g.out = nullptr;
+  g.out_acc = dW;
+  g.Mo = N;
+  g.No = K;
+  g.Kc = M;
+  return gemm_common("fp8bw_gemm_wgrad_acc_f32", g, stream);
 }
 
 // ============================================================ MXFP8 grouped GEMM

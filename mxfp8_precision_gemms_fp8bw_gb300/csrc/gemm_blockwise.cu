@@ -121,7 +121,8 @@ __device__ __forceinline__ void promote_per_column(SharedStorage& sm, uint32_t t
                                                    int lane, int num_tiles, int num_m, int num_n, int num_k,
                                                    const float* __restrict__ sa, int64_t sa_ld,
                                                    const float* __restrict__ sb, int64_t sb_ld_kb,
-                                                   uint16_t* __restrict__ out, int No, int* status, AbortFlag ab) {
+                                                   uint16_t* __restrict__ out, float* __restrict__ out_acc, int No,
+                                                   int* status, AbortFlag ab) {
   const int q4 = lane & 3, r8 = lane >> 2;
   int buf = 0;
   uint32_t tphase = 0;
@@ -209,15 +210,32 @@ __device__ __forceinline__ void promote_per_column(SharedStorage& sm, uint32_t t
       }
     }
     if (!alive) break;
+    if (out_acc != nullptr) {
+      // Gradient accumulation: add the tile to the caller's fp32 dW.
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < 2; ++h) {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        uint32_t* orow = reinterpret_cast<uint32_t*>(out + (rbase + 16 * h + 8 * e) * No + col0 + 2 * q4);
+        for (int e = 0; e < 2; ++e) {
+          float2* orow = reinterpret_cast<float2*>(out_acc + (rbase + 16 * h + 8 * e) * No + col0 + 2 * q4);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float2 v = acc[(h * 16 + k) * 2 + e];
-          orow[4 * k] = pack_bf16x2(v.x, v.y);
+          for (int k = 0; k < 16; ++k) {
+            const float2 v = acc[(h * 16 + k) * 2 + e];
+            const float2 o = orow[4 * k];
+            orow[4 * k] = make_float2(o.x + v.x, o.y + v.y);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          uint32_t* orow = reinterpret_cast<uint32_t*>(out + (rbase + 16 * h + 8 * e) * No + col0 + 2 * q4);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float2 v = acc[(h * 16 + k) * 2 + e];
+            orow[4 * k] = pack_bf16x2(v.x, v.y);
+          }
         }
       }
     }
@@ -228,7 +246,8 @@ template <int kBScale>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     blockwise_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                           const float* __restrict__ sa, int64_t sa_ld, const float* __restrict__ sb, int64_t sb_ld_nb,
-                          int64_t sb_ld_kb, uint16_t* __restrict__ out, int Mo, int No, int Kc, int* status) {
+                          int64_t sb_ld_kb, uint16_t* __restrict__ out, float* __restrict__ out_acc, int Mo, int No,
+                          int Kc, int* status) {
   extern __shared__ uint8_t smem_raw[];
   SharedStorage& sm =
       *reinterpret_cast<SharedStorage*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -358,7 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3;              // TMEM lane quarter this warp may access
     if constexpr (kBScale == 1) {
       promote_per_column(sm, tmem, ew, half, quarter, lane, num_tiles, num_m, num_n, num_k, sa, sa_ld, sb, sb_ld_kb,
-                         out, No, status, ab);
+                         out, out_acc, No, status, ab);
     } else {
       const int row = quarter * 32 + lane;       // row of the tile this thread owns
       const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
@@ -479,7 +498,7 @@ cudaError_t launch_blockwise_gemm(const BlockwiseGemmArgs& g, cudaStream_t st) {
                              static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     blockwise_gemm_kernel<0><<<grid, NUM_THREADS, kSmemBytes, st>>>(ta, tb, g.sa, g.sa_ld, g.sb, g.sb_ld_nb, g.sb_ld_kb,
-                                                                    g.out, static_cast<int>(g.Mo),
+                                                                    g.out, g.out_acc, static_cast<int>(g.Mo),
                                                                     static_cast<int>(g.No), static_cast<int>(g.Kc),
                                                                     g.status);
   } else {
@@ -487,7 +506,7 @@ cudaError_t launch_blockwise_gemm(const BlockwiseGemmArgs& g, cudaStream_t st) {
                              static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     blockwise_gemm_kernel<1><<<grid, NUM_THREADS, kSmemBytes, st>>>(ta, tb, g.sa, g.sa_ld, g.sb, g.sb_ld_nb, g.sb_ld_kb,
-                                                                    g.out, static_cast<int>(g.Mo),
+                                                                    g.out, g.out_acc, static_cast<int>(g.Mo),
                                                                     static_cast<int>(g.No), static_cast<int>(g.Kc),
                                                                     g.status);
   }

@@ -35,7 +35,8 @@ struct BlockwiseGemmArgs {
   int64_t sb_ld_nb;   // kBlock128x128: stride between 128-row blocks of B
   int64_t sb_ld_kb;   // stride between contraction blocks
   BScale b_scale;
-  uint16_t* out;      // [Mo, No] bf16
+  uint16_t* out;      // [Mo, No] bf16 (unused when out_acc is set)
+  float* out_acc;     // kPerRow only, may be null: out_acc[Mo, No] += result in fp32
   int64_t Mo, No, Kc;
   int* status;
   int num_sms;

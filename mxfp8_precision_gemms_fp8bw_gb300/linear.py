@@ -48,9 +48,11 @@ def forward(x: torch.Tensor, wq: QuantizedWeight, stream=None):
     return y, (xqT, xsT)
 
 
-def backward(dy: torch.Tensor, x_col, wq: QuantizedWeight, stream=None):
+def backward(dy: torch.Tensor, x_col, wq: QuantizedWeight, stream=None, dW_acc: torch.Tensor | None = None):
     """dx = dy W and dW = dy^T x.  x_col is (q_x^T, s_x^T) from forward, or
-    the bf16 x itself (then quantized colwise here).  Returns (dx, dW)."""
+    the bf16 x itself (then quantized colwise here).  Returns (dx, dW); with
+    an fp32 ``dW_acc`` [N, K] the gradient is added to it instead (gradient
+    accumulation) and dW_acc is returned as dW."""
     M, N = dy.shape
     if isinstance(x_col, torch.Tensor):
         xqT, xsT = B.alloc_quant_1x128_col(x_col)
@@ -63,6 +65,9 @@ def backward(dy: torch.Tensor, x_col, wq: QuantizedWeight, stream=None):
     B.fp8bw_quant_1x128_rowcol(dy, dyq, dys, dyqT, dysT, stream)
     dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device)
     B.fp8bw_gemm_dgrad(dyq, dys, wq.qT, wq.s, dx, stream)
+    if dW_acc is not None:
+        B.fp8bw_gemm_wgrad_acc_f32(dyqT, dysT, xqT, xsT, dW_acc, stream)
+        return dx, dW_acc
     dW = torch.empty((N, K), dtype=torch.bfloat16, device=dy.device)
     B.fp8bw_gemm_wgrad(dyqT, dysT, xqT, xsT, dW, stream)
     return dx, dW

@@ -139,3 +139,20 @@ def test_full_size_moe_sampled():
     k_sel = np.sort(rng.choice(K, 128, replace=False))
     e = grouped_errors(t.x, t.w, t.dy, t.group_end, y, dx, dW, rows=rows, n_sel=n_sel, k_sel=k_sel)
     assert max(e) <= TOL, e
+
+
+def test_full_size_mxfp8_dense_linear_sampled():
+    """The MXFP8 dense linear (the grouped path with one group, the mxfp8
+    recipe of PR #3037's "Microbenchmarks" comparison) on the dense workload's
+    x, W, dy (M=16384, K=5120, N=8192), checked on sampled rows and columns."""
+    t = inputs.dense()
+    M, K = t.x.shape
+    N = t.w.shape[0]
+    w3 = t.w.reshape(1, N, K)
+    y, dx, dW = gpu_moe(t.x, w3, t.dy, [M])
+    rng = np.random.default_rng(2)
+    rows = np.sort(rng.choice(M, 256, replace=False))
+    n_sel = np.sort(rng.choice(N, 128, replace=False))
+    k_sel = np.sort(rng.choice(K, 128, replace=False))
+    e = grouped_errors(t.x, w3, t.dy, np.array([M]), y, dx, dW, rows=rows, n_sel=n_sel, k_sel=k_sel)
+    assert max(e) <= TOL, e
