@@ -33,6 +33,7 @@
 //
 // Every wait is bounded (see mbar_wait): a lost arrival makes the kernel
 // record a timeout in the device error word and unwind, freeing its TMEM.
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -51,6 +52,9 @@ constexpr int NUM_EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;  // two BN-column fp32 partial buffers
 constexpr int GROUP_M = 16;          // tile raster: 16 row-blocks share a column sweep
 constexpr int SB_STRIDE = 36;        // floats per lane-quarter row of the staged column scales
+constexpr int EPI_BOX_ROWS = 16;     // output staging box: 16 rows x 64 bf16 columns (128 B rows)
+constexpr int EPI_BOX_COLS = 64;
+constexpr int EPI_BOX_BYTES = EPI_BOX_ROWS * EPI_BOX_COLS * 2;
 // Register split.  Each SM sub-partition holds one warp of every warpgroup and
 // 16384 registers, so a 384-thread CTA launches with 168 per thread; warpgroup
 // 0 (producer, MMA, TMEM owner) then gives up registers to warpgroups 1-2
@@ -67,6 +71,9 @@ struct RegSplit {
 struct SharedStorage {
   uint8_t a[STAGES][A_BYTES];  // each stage 1024-byte aligned (swizzle atom)
   uint8_t b[STAGES][B_BYTES];
+  // Output staging, one 16-row x 64-column bf16 box (2 KB, chunks swizzled
+  // by row) per promotion warp.
+  uint8_t epi[NUM_EPI_WARPS][EPI_BOX_BYTES];
   // Per-column B scales of the current and next block, private to each
   // promotion warp: [warp][buffer][SB_STRIDE * q + 2 * chunk + e] holds column
   // 8 * chunk + 2 * q + e (q = lane % 4), so a thread's 32 scales are
@@ -104,8 +111,44 @@ __device__ __forceinline__ void sts_f32x2(uint32_t addr, float a, float b) {
   asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 
-__device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+// Byte offset of 16-byte chunk k (0..7) of row r in a box of 128-byte rows
+// written for a 128-byte-swizzled TMA map: chunk k of row r sits at chunk
+// k ^ (r % 8), which also spreads a warp's writes over all banks.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int k) {
+  return static_cast<uint32_t>(r * 128 + ((k ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
+                                             uint32_t f, uint32_t g, uint32_t h) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d),
+               "r"(e), "r"(f), "r"(g), "r"(h)
+               : "memory");
+}
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+// Writes a staged 16-row x 64-column bf16 box (rows of 128 bytes, chunk k of
+// row r at chunk k ^ (r % 8)) to out[row0 + r][col0 + c]: each warp store
+// covers four whole 128-byte row segments.
+__device__ __forceinline__ void store_box(uint32_t stage, uint16_t* __restrict__ out, int64_t ld, int64_t row0,
+                                          int64_t col0, int lane) {
+  const int k = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 4 * i + (lane >> 3);
+    const uint4 v = lds_v4(stage + sw128_offset(r, k));
+    uint16_t* p = out + (row0 + r) * ld + col0 + 8 * k;
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+  }
+}
+
+__device__ __forceinline__ void sts_b32(uint32_t addr, uint32_t a) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
 }
 
 // Promotion with a per-column B scale (wgrad: both operands in 1x128 blocks
@@ -226,16 +269,26 @@ __device__ __forceinline__ void promote_per_column(SharedStorage& sm, uint32_t t
         }
       }
     } else {
+      // Four 16-row x 64-column boxes per warp (lane half h, column half cc),
+      // staged through the warp's swizzled buffer for whole-line stores.
+      const uint32_t stage = smem_u32(sm.epi[ew]);
+      const int64_t row0 = static_cast<int64_t>(mb) * BM + quarter * 32;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          uint32_t* orow = reinterpret_cast<uint32_t*>(out + (rbase + 16 * h + 8 * e) * No + col0 + 2 * q4);
+        for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float2 v = acc[(h * 16 + k) * 2 + e];
-            orow[4 * k] = pack_bf16x2(v.x, v.y);
+          for (int e = 0; e < 2; ++e) {
+            const int r = 8 * e + r8;  // row within the box
+#pragma unroll
+            for (int k8 = 0; k8 < 8; ++k8) {
+              const float2 v = acc[(h * 16 + cc * 8 + k8) * 2 + e];
+              sts_b32(stage + sw128_offset(r, k8) + 4 * q4, pack_bf16x2(v.x, v.y));
+            }
           }
+          __syncwarp();
+          store_box(stage, out, No, row0 + h * 16, col0 + cc * EPI_BOX_COLS, lane);
+          __syncwarp();
         }
       }
     }
@@ -447,11 +500,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         if (!alive) break;
+        // Output: the thread's row, 128 bf16 columns, as eight 32-byte stores
+        // (each a whole sector).
         uint16_t* orow = out + m * No + col0;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          st_global_v4(orow + c * 8, pack_bf16x2(acc[4 * c].x, acc[4 * c].y), pack_bf16x2(acc[4 * c + 1].x, acc[4 * c + 1].y),
-                       pack_bf16x2(acc[4 * c + 2].x, acc[4 * c + 2].y), pack_bf16x2(acc[4 * c + 3].x, acc[4 * c + 3].y));
+        for (int c = 0; c < 8; ++c) {
+          const int j = 8 * c;
+          st_global_v8(orow + 16 * c, pack_bf16x2(acc[j].x, acc[j].y), pack_bf16x2(acc[j + 1].x, acc[j + 1].y),
+                       pack_bf16x2(acc[j + 2].x, acc[j + 2].y), pack_bf16x2(acc[j + 3].x, acc[j + 3].y),
+                       pack_bf16x2(acc[j + 4].x, acc[j + 4].y), pack_bf16x2(acc[j + 5].x, acc[j + 5].y),
+                       pack_bf16x2(acc[j + 6].x, acc[j + 6].y), pack_bf16x2(acc[j + 7].x, acc[j + 7].y));
         }
       }
     }
