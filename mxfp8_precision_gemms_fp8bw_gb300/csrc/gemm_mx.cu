@@ -451,10 +451,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       if (store) {
+        // Eight 32-byte stores: each lane writes whole sectors of its row.
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(orow + c * 8), "r"(v[4 * c]),
-                       "r"(v[4 * c + 1]), "r"(v[4 * c + 2]), "r"(v[4 * c + 3])
+        for (int c = 0; c < 8; ++c) {
+          asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(orow + c * 16),
+                       "r"(v[8 * c]), "r"(v[8 * c + 1]), "r"(v[8 * c + 2]), "r"(v[8 * c + 3]), "r"(v[8 * c + 4]),
+                       "r"(v[8 * c + 5]), "r"(v[8 * c + 6]), "r"(v[8 * c + 7])
                        : "memory");
         }
       }
