@@ -270,23 +270,30 @@ def run_ours(args, world, rank, local):
                 "unit": "TFLOP/s", "frac": round(dom_ach / fp8_peak, 4), "traffic": traffic,
                 "peak_source": f"{peaks['source']} sustained bf16 x {FP8_OVER_BF16:g} (nominal fp8/bf16 ratio)"}
 
-    # End to end through the public API with host buffers: H2D of the step's
-    # inputs from pinned memory, the step, D2H of its three outputs.
+    # End to end through the public API with host buffers: every step copies
+    # its inputs from pinned memory, runs, and copies y, dx, dW back, with the
+    # copies of neighbouring steps overlapping the kernels (PipelinedLinearSteps).
+    from mxfp8_precision_gemms_fp8bw_gb300.linear import PipelinedLinearSteps
     y_h = torch.empty((M, N), dtype=torch.bfloat16, pin_memory=True)
     dx_h = torch.empty((M, K), dtype=torch.bfloat16, pin_memory=True)
     dW_h = torch.empty((N, K), dtype=torch.bfloat16, pin_memory=True)
-    e2e_steps = max(1, min(args.steps, 10))
+    pipe = PipelinedLinearSteps(M, N, K, device=dev)
+    e2e_steps = max(1, min(args.steps, 20))
     for _ in range(2):
-        _e2e_step(x, w, dy, x_h, w_h, dy_h, ws, y_h, dx_h, dW_h)
+        pipe.step(x_h, w_h, dy_h, y_h, dx_h, dW_h)
+    pipe.synchronize()
     torch.cuda.synchronize(dev)
     barrier(world)
+    # the first upload starts after e0 (upload stream); the last download ends before e1
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(pipe.up)
     for _ in range(e2e_steps):
-        _e2e_step(x, w, dy, x_h, w_h, dy_h, ws, y_h, dx_h, dW_h)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+        pipe.step(x_h, w_h, dy_h, y_h, dx_h, dW_h)
+    pipe.down.wait_stream(pipe.comp)
+    e1.record(pipe.down)
+    pipe.synchronize()
     e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / e2e_steps, dev)
+    del pipe
     h2d = (x.numel() + w.numel() + dy.numel()) * 2
     d2h = (y_h.numel() + dx_h.numel() + dW_h.numel()) * 2
 
@@ -419,16 +426,6 @@ def run_moe(dev, steps, warmup, fp8_peak, hbm_peak, world, dense: bool = False):
         "kernels": kernel_table(per, algo, fp8_peak, hbm_peak),
         "linear_us": linear_us(per, ["mx_quant_1x32_row(x)", "mx_quant_1x32_row(W)", "mx_grouped_fwd"]),
     }
-
-
-def _e2e_step(x, w, dy, x_h, w_h, dy_h, ws, y_h, dx_h, dW_h):
-    x.copy_(x_h, non_blocking=True)
-    w.copy_(w_h, non_blocking=True)
-    dy.copy_(dy_h, non_blocking=True)
-    y, dx, dW = ws.step(x, w, dy)
-    y_h.copy_(y, non_blocking=True)
-    dx_h.copy_(dx, non_blocking=True)
-    dW_h.copy_(dW, non_blocking=True)
 
 
 def load_traffic(kernel: str):

@@ -274,3 +274,62 @@ class MxMoEWorkspace:
             "mx_quant_1x32_col(x)": ("bytes", mx(M, K)),
             "mx_grouped_wgrad": ("flops", 2 * M * N * K),
         }
+
+
+class PipelinedLinearSteps:
+    """Forward+backward steps of a blockwise-FP8 linear fed from and drained to
+    pinned host memory, with the copies of neighbouring steps overlapping the
+    kernels.
+
+    Step i uses device buffer set i % 2: its inputs are copied host->device on
+    an upload stream, the six library calls of ``BlockwiseLinearWorkspace.step``
+    run on a compute stream once they have landed, and y, dx, dW are copied
+    device->host on a download stream once computed.  Events order each use of
+    a buffer set after the previous step that used it (upload after that
+    step's kernels read the inputs, kernels after that step's download read
+    the outputs), so step i + 1's upload and step i - 1's download run while
+    step i computes.
+    """
+
+    def __init__(self, M: int, N: int, K: int, device="cuda"):
+        bf = torch.bfloat16
+        e = lambda shape: torch.empty(shape, dtype=bf, device=device)  # noqa: E731
+        self.inputs = [(e((M, K)), e((N, K)), e((M, N))) for _ in range(2)]
+        self.ws = [BlockwiseLinearWorkspace(M, N, K, device=device) for _ in range(2)]
+        self.up, self.comp, self.down = (torch.cuda.Stream(device=device) for _ in range(3))
+        mk = lambda: [torch.cuda.Event() for _ in range(2)]  # noqa: E731
+        self.uploaded, self.computed, self.downloaded = mk(), mk(), mk()
+        self.i = 0
+
+    def step(self, x_h, w_h, dy_h, y_h, dx_h, dW_h) -> None:
+        """Enqueues one step: host inputs x_h, w_h, dy_h (pinned bf16) in,
+        host outputs y_h, dx_h, dW_h (pinned bf16) out.  Returns at once;
+        ``synchronize`` waits for every enqueued step."""
+        for name, t in (("x_h", x_h), ("w_h", w_h), ("dy_h", dy_h), ("y_h", y_h), ("dx_h", dx_h), ("dW_h", dW_h)):
+            if t.device.type != "cpu" or not t.is_pinned():
+                raise ValueError(f"{name} must be a pinned host tensor")
+        s = self.i % 2
+        x, w, dy = self.inputs[s]
+        ws = self.ws[s]
+        if self.i >= 2:
+            self.up.wait_event(self.computed[s])
+            self.comp.wait_event(self.downloaded[s])
+        with torch.cuda.stream(self.up):
+            x.copy_(x_h, non_blocking=True)
+            w.copy_(w_h, non_blocking=True)
+            dy.copy_(dy_h, non_blocking=True)
+            self.uploaded[s].record(self.up)
+        self.comp.wait_event(self.uploaded[s])
+        ws.step(x, w, dy, stream=self.comp)
+        self.computed[s].record(self.comp)
+        self.down.wait_event(self.computed[s])
+        with torch.cuda.stream(self.down):
+            y_h.copy_(ws.y, non_blocking=True)
+            dx_h.copy_(ws.dx, non_blocking=True)
+            dW_h.copy_(ws.dW, non_blocking=True)
+            self.downloaded[s].record(self.down)
+        self.i += 1
+
+    def synchronize(self) -> None:
+        for st in (self.up, self.comp, self.down):
+            st.synchronize()
