@@ -14,11 +14,13 @@
 // Kernel structure (one persistent CTA per SM, 384 threads):
 //   warp 0      TMA producer: A tile 128x128 and B tile 256x128 (e4m3,
 //               128-byte swizzle) per contraction block into a 4-stage ring.
-//   warp 1      allocates / frees the 512 TMEM columns; one thread issues 4
-//               tcgen05.mma (K = 32 each) per block into one of two 128x256
-//               fp32 TMEM partial buffers, then commits to the smem ring's
-//               "empty" barrier and to the buffer's "full" barrier.
-//   warps 2-3   idle (they complete warpgroup 0, which gives its registers
+//   warps 1-2   warp 1 allocates / frees the 512 TMEM columns; one thread
+//               of each issues 4 tcgen05.mma (K = 32 each) per block, warp 1
+//               for the even blocks into TMEM partial buffer 0, warp 2 for
+//               the odd ones into buffer 1 (128x256 fp32 each), then commits
+//               to the smem ring's "empty" barrier and to the buffer's "full"
+//               barrier.
+//   warp 3      idle (it completes warpgroup 0, which gives its registers
 //               to the promotion warpgroups).
 //   warps 4-11  promotion + epilogue: warp w reads TMEM lanes 32*(w%4)...,
 //               warps 4-7 columns 0-127 and warps 8-11 columns 128-255 of the
@@ -83,7 +85,7 @@ struct SharedStorage {
   uint64_t empty[STAGES];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
-  uint64_t mma_drain;          // used only when unwinding after a timeout
+  uint64_t mma_drain[2];       // used only when unwinding after a timeout
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -181,15 +183,15 @@ __device__ __forceinline__ void promote_per_column(SharedStorage& sm, uint32_t t
 
     // Scales of the next block are fetched one block ahead; each lane fetches
     // four consecutive column scales of the warp's 128 (one coalesced 512-byte
-    // row per warp) and stages them in the warp's own shared buffer.
-    float sa_next[4];  // [h * 2 + e]
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sa_next[i] = __ldg(sa + rbase + 16 * (i >> 1) + 8 * (i & 1));
+    // row per warp) and stages them in the warp's own shared buffer, and the
+    // A scale of one of the warp's 32 rows, which shuffles hand to the four
+    // threads holding that row (one global load per lane instead of four).
+    float sa_lane = __ldg(sa + (rbase - r8) + lane);
     float4 sb4_next = __ldg(reinterpret_cast<const float4*>(sb + col0) + lane);
     for (int kb = 0; kb < num_k; ++kb) {
       float sa_cur[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) sa_cur[i] = sa_next[i];
+      for (int i = 0; i < 4; ++i) sa_cur[i] = __shfl_sync(0xffffffffu, sa_lane, r8 + 16 * (i >> 1) + 8 * (i & 1));
       // The buffer written now was last read two blocks ago; every lane
       // finished those reads before the previous block's __syncwarp.
       {
@@ -202,8 +204,7 @@ __device__ __forceinline__ void promote_per_column(SharedStorage& sm, uint32_t t
       __syncwarp();
       if (kb + 1 < num_k) {
         const float* sak = sa + static_cast<int64_t>(kb + 1) * sa_ld;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) sa_next[i] = __ldg(sak + rbase + 16 * (i >> 1) + 8 * (i & 1));
+        sa_lane = __ldg(sak + (rbase - r8) + lane);
         sb4_next = __ldg(reinterpret_cast<const float4*>(sb + static_cast<int64_t>(kb + 1) * sb_ld_kb + col0) + lane);
       }
       if (!mbar_wait(&sm.tmem_full[buf], tphase, ab, status)) {
@@ -318,7 +319,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&sm.tmem_full[b], 1);
       mbar_init(&sm.tmem_empty[b], NUM_EPI_WARPS);
     }
-    mbar_init(&sm.mma_drain, 1);
+    mbar_init(&sm.mma_drain[0], 1);
+    mbar_init(&sm.mma_drain[1], 1);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -379,16 +381,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two issuing threads: warp 1 issues the even contraction blocks (into
+    // TMEM buffer 0), warp 2 the odd ones (buffer 1), so the MMAs of block
+    // g + 2 go out as soon as the promotion hands buffer g % 2 back, even
+    // while the other issuer is still feeding block g + 1 to the tensor core.
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
-      int stage = 0, buf = 0;
-      uint32_t phase = 0, tphase = 0;
+      const int me = warp - 1;
+      const uint32_t d_tmem = tmem + static_cast<uint32_t>(me * BN);
       bool alive = true;
+      uint32_t g = 0;  // running block index over this CTA's tiles
       for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
-        for (int kb = 0; kb < num_k; ++kb) {
-          if (!mbar_wait(&sm.tmem_empty[buf], tphase ^ 1u, ab, status) ||
+        for (int kb = 0; kb < num_k; ++kb, ++g) {
+          if ((g & 1u) != static_cast<uint32_t>(me)) continue;
+          const int stage = static_cast<int>(g % STAGES);
+          const uint32_t phase = (g / STAGES) & 1u;
+          const uint32_t tphase = (g >> 1) & 1u;
+          if (!mbar_wait(&sm.tmem_empty[me], tphase ^ 1u, ab, status) ||
               !mbar_wait(&sm.full[stage], phase, ab, status)) {
             alive = false;
             break;
@@ -396,29 +407,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t a_addr = smem_u32(sm.a[stage]);
           const uint32_t b_addr = smem_u32(sm.b[stage]);
-          const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * BN);
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k) {
             mma_e4m3(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32), sdesc_kmajor_sw128(b_addr + k * 32), idesc,
                      k > 0 ? 1u : 0u);
           }
           mma_commit(&sm.empty[stage]);
-          mma_commit(&sm.tmem_full[buf]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          if (++buf == 2) {
-            buf = 0;
-            tphase ^= 1u;
-          }
+          mma_commit(&sm.tmem_full[me]);
         }
       }
       if (!alive) {
-        // Unwinding: wait for the MMAs already issued before TMEM is freed.
-        mma_commit(&sm.mma_drain);
+        // Unwinding: wait for this thread's MMAs already issued before TMEM is freed.
+        mma_commit(&sm.mma_drain[me]);
         int dummy = 0;
-        mbar_wait(&sm.mma_drain, 0, AbortFlag{&dummy}, status, 1000000ull);
+        mbar_wait(&sm.mma_drain[me], 0, AbortFlag{&dummy}, status, 1000000ull);
       }
     }
   }
