@@ -13,7 +13,8 @@
 //
 // Kernel structure (one persistent CTA per SM, 384 threads):
 //   warp 0      TMA producer: A tile 128x128 and B tile 256x128 (e4m3,
-//               128-byte swizzle) per contraction block into a 4-stage ring.
+//               128-byte swizzle) per contraction block into a ring of 3
+//               stages (one B scale per block) or 4 (per-column B scale).
 //   warps 1-2   warp 1 allocates / frees the 512 TMEM columns; one thread
 //               of each issues 4 tcgen05.mma (K = 32 each) per block, warp 1
 //               for the even blocks into TMEM partial buffer 0, warp 2 for
@@ -28,9 +29,12 @@
 //               thread, release the buffer, and after the last block write
 //               their part of the bf16 output tile.  With one B scale per
 //               128x128 block (fwd, dgrad) a thread owns one row (32x32b
-//               TMEM loads); with one B scale per column (wgrad) a thread
-//               owns 4 rows x 32 columns (16x256b loads), which divides the
-//               broadcast reads of the column scales by four.
+//               TMEM loads) and the warp's 32 x 128 output slice leaves
+//               through its shared staging area by two TMA stores that
+//               complete while the warp promotes the next tile; with one B
+//               scale per column (wgrad) a thread owns 4 rows x 32 columns
+//               (16x256b loads), which divides the broadcast reads of the
+//               column scales by four.
 // The MMA of block kb+1 runs while block kb is being promoted.
 //
 // Every wait is bounded (see mbar_wait): a lost arrival makes the kernel
@@ -45,7 +49,6 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 128;
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int NUM_THREADS = 384;
@@ -70,19 +73,23 @@ struct RegSplit {
   static_assert(ctrl + 2 * epi <= 3 * 168, "register split exceeds the launch budget");
 };
 
-struct SharedStorage {
-  uint8_t a[STAGES][A_BYTES];  // each stage 1024-byte aligned (swizzle atom)
-  uint8_t b[STAGES][B_BYTES];
-  // Output staging, one 16-row x 64-column bf16 box (2 KB, chunks swizzled
-  // by row) per promotion warp.
-  uint8_t epi[NUM_EPI_WARPS][EPI_BOX_BYTES];
+template <int kBScale>
+struct SharedStorageT {
+  // fwd/dgrad: 3 stages and an 8 KB output staging area per promotion warp
+  // (its 32 rows x 128 columns as two 32 x 64 boxes for TMA stores);
+  // wgrad: 4 stages and one 16 x 64 box (2 KB) per warp.
+  static constexpr int S = kBScale == 0 ? 3 : 4;
+  static constexpr int EPI = kBScale == 0 ? 8192 : EPI_BOX_BYTES;
+  uint8_t a[S][A_BYTES];  // each stage 1024-byte aligned (swizzle atom)
+  uint8_t b[S][B_BYTES];
+  uint8_t epi[NUM_EPI_WARPS][EPI];
   // Per-column B scales of the current and next block, private to each
   // promotion warp: [warp][buffer][SB_STRIDE * q + 2 * chunk + e] holds column
   // 8 * chunk + 2 * q + e (q = lane % 4), so a thread's 32 scales are
   // contiguous and its 16-byte loads of two chunks hit distinct banks.
   float sb_vec[NUM_EPI_WARPS][2][4 * SB_STRIDE];
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[S];
+  uint64_t empty[S];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t mma_drain[2];       // used only when unwinding after a timeout
@@ -90,7 +97,24 @@ struct SharedStorage {
   int abort_flag;
 };
 
-constexpr size_t kSmemBytes = sizeof(SharedStorage) + 1024;
+template <int kBScale>
+constexpr size_t smem_bytes() {
+  return sizeof(SharedStorageT<kBScale>) + 1024;
+}
+
+// TMA bulk tensor store of a box from shared memory (128-byte swizzle) and
+// the bulk async-group bookkeeping around it.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map), "r"(src),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
   const int group_size = GROUP_M * num_n;
@@ -162,7 +186,7 @@ __device__ __forceinline__ void sts_b32(uint32_t addr, uint32_t a) {
 // contiguous: one conflict-free 16-byte shared load covers two chunks for
 // both lane halves (8 loads per thread per block).  Shared-memory loads
 // compete with the tensor core's operand reads, so they are kept this few.
-__device__ __forceinline__ void promote_per_column(SharedStorage& sm, uint32_t tmem, int ew, int half, int quarter,
+__device__ __forceinline__ void promote_per_column(SharedStorageT<1>& sm, uint32_t tmem, int ew, int half, int quarter,
                                                    int lane, int num_tiles, int num_m, int num_n, int num_k,
                                                    const float* __restrict__ sa, int64_t sa_ld,
                                                    const float* __restrict__ sb, int64_t sb_ld_kb,
@@ -299,12 +323,15 @@ __device__ __forceinline__ void promote_per_column(SharedStorage& sm, uint32_t t
 template <int kBScale>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     blockwise_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+                          const __grid_constant__ CUtensorMap tma_out,
                           const float* __restrict__ sa, int64_t sa_ld, const float* __restrict__ sb, int64_t sb_ld_nb,
                           int64_t sb_ld_kb, uint16_t* __restrict__ out, float* __restrict__ out_acc, int Mo, int No,
                           int Kc, int* status) {
   extern __shared__ uint8_t smem_raw[];
-  SharedStorage& sm =
-      *reinterpret_cast<SharedStorage*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  using Storage = SharedStorageT<kBScale>;
+  constexpr int STAGES = Storage::S;
+  Storage& sm =
+      *reinterpret_cast<Storage*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_m = Mo / BM, num_n = No / BN, num_k = Kc / BK;
   const int num_tiles = num_m * num_n;
@@ -502,18 +529,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         if (!alive) break;
-        // Output: the thread's row, 128 bf16 columns, as eight 32-byte stores
-        // (each a whole sector).
-        uint16_t* orow = out + m * No + col0;
+        // Output: the warp's 32 rows x 128 columns go through its staging
+        // area (two 32 x 64 boxes, 128-byte swizzle) to two TMA stores, which
+        // complete while the warp promotes the next tile.
+        const uint32_t stage = smem_u32(sm.epi[ew]);
+        if (lane == 0) bulk_wait_read_all();  // the previous tile's stores have read the area
+        __syncwarp();
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int j = 8 * c;
-          st_global_v8(orow + 16 * c, pack_bf16x2(acc[j].x, acc[j].y), pack_bf16x2(acc[j + 1].x, acc[j + 1].y),
-                       pack_bf16x2(acc[j + 2].x, acc[j + 2].y), pack_bf16x2(acc[j + 3].x, acc[j + 3].y),
-                       pack_bf16x2(acc[j + 4].x, acc[j + 4].y), pack_bf16x2(acc[j + 5].x, acc[j + 5].y),
-                       pack_bf16x2(acc[j + 6].x, acc[j + 6].y), pack_bf16x2(acc[j + 7].x, acc[j + 7].y));
+        for (int c = 0; c < 16; ++c) {
+          const int j = 4 * c;
+          sts_v4(stage + (c >> 3) * 4096 + sw128_offset(lane, c & 7), pack_bf16x2(acc[j].x, acc[j].y),
+                 pack_bf16x2(acc[j + 1].x, acc[j + 1].y), pack_bf16x2(acc[j + 2].x, acc[j + 2].y),
+                 pack_bf16x2(acc[j + 3].x, acc[j + 3].y));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int32_t r0 = mb * BM + quarter * 32;
+          tma_store_2d(&tma_out, stage, static_cast<int32_t>(col0), r0);
+          tma_store_2d(&tma_out, stage + 4096, static_cast<int32_t>(col0) + 64, r0);
+          bulk_commit();
         }
       }
+      if (lane == 0) bulk_wait_all();  // this warp's stores are done before the CTA ends
     }
   }
 
@@ -546,26 +584,42 @@ bool encode_kmajor_u8(CUtensorMap* map, const void* base, int64_t rows, int64_t 
 
 }  // namespace
 
+// 2D map over the row-major [rows, cols] bf16 output, box 32 rows x 64
+// columns (128 bytes), 128-byte swizzle.
+bool encode_out_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
+  auto fn = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64u, 32u};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_blockwise_gemm(const BlockwiseGemmArgs& g, cudaStream_t st) {
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, to;
   if (!encode_kmajor_u8(&ta, g.a, g.Mo, g.Kc, BM) || !encode_kmajor_u8(&tb, g.b, g.No, g.Kc, BN))
     return cudaErrorInvalidValue;
+  if (g.b_scale == BScale::kBlock128x128 && !encode_out_bf16(&to, g.out, g.Mo, g.No)) return cudaErrorInvalidValue;
+  if (g.b_scale != BScale::kBlock128x128) to = ta;  // unused by the per-column kernel
   const int num_tiles = static_cast<int>((g.Mo / BM) * (g.No / BN));
   const int grid = num_tiles < g.num_sms ? num_tiles : g.num_sms;
   cudaError_t e;
   if (g.b_scale == BScale::kBlock128x128) {
     e = cudaFuncSetAttribute(blockwise_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes));
+                             static_cast<int>(smem_bytes<0>()));
     if (e != cudaSuccess) return e;
-    blockwise_gemm_kernel<0><<<grid, NUM_THREADS, kSmemBytes, st>>>(ta, tb, g.sa, g.sa_ld, g.sb, g.sb_ld_nb, g.sb_ld_kb,
+    blockwise_gemm_kernel<0><<<grid, NUM_THREADS, smem_bytes<0>(), st>>>(ta, tb, to, g.sa, g.sa_ld, g.sb, g.sb_ld_nb, g.sb_ld_kb,
                                                                     g.out, g.out_acc, static_cast<int>(g.Mo),
                                                                     static_cast<int>(g.No), static_cast<int>(g.Kc),
                                                                     g.status);
   } else {
     e = cudaFuncSetAttribute(blockwise_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes));
+                             static_cast<int>(smem_bytes<1>()));
     if (e != cudaSuccess) return e;
-    blockwise_gemm_kernel<1><<<grid, NUM_THREADS, kSmemBytes, st>>>(ta, tb, g.sa, g.sa_ld, g.sb, g.sb_ld_nb, g.sb_ld_kb,
+    blockwise_gemm_kernel<1><<<grid, NUM_THREADS, smem_bytes<1>(), st>>>(ta, tb, to, g.sa, g.sa_ld, g.sb, g.sb_ld_nb, g.sb_ld_kb,
                                                                     g.out, g.out_acc, static_cast<int>(g.Mo),
                                                                     static_cast<int>(g.No), static_cast<int>(g.Kc),
                                                                     g.status);
