@@ -190,7 +190,7 @@ def sample_desc(rows, w_rows):
 
 
 REF_SAMPLE = (128, 1024)      # per step of --impl reference (about a second)
-BASELINE_SAMPLE = (256, 8192)  # cpu_baseline of the GPU arm (tens of seconds of CPU work)
+CPU_SAMPLE = (256, 8192)  # cpu_baseline of the GPU arm (tens of seconds of CPU work)
 
 
 def run_reference(args, world, rank):
@@ -304,7 +304,7 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rows, w_rows = BASELINE_SAMPLE
+        rows, w_rows = CPU_SAMPLE
         secs, flops, threads = oracle_sample(rows, w_rows)
         cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": sample_desc(rows, w_rows), "seconds": round(secs, 2)}

@@ -3,7 +3,8 @@
 Bar: max over elements of |out - ref| / (||a_i|| ||b_j||) <= 2e-3 (the
 oracle's GEMM_TOL; bf16 output rounding alone contributes up to 2^-9), and
 end-to-end SQNR >= 25 dB against the product of the unquantized bf16 inputs.
-Shapes span one tile, several tiles with more tiles than SMs, the tiny
+Shapes span one tile, several tiles with more tiles than SMs, an odd number
+of contraction blocks (wgrad over M = 384) with more tiles than SMs, the tiny
 workload, and the full-size dense workload on sampled output rows.
 """
 import numpy as np
@@ -72,7 +73,7 @@ def test_tiny_linear_fwd_bwd():
 
 
 @pytest.mark.parametrize("M,N,K,seed", [(128, 256, 256, 0), (384, 512, 768, 1), (256, 768, 1280, 2),
-                                        (2048, 4096, 512, 3)])
+                                        (2048, 4096, 512, 3), (384, 4096, 1536, 4)])
 def test_linear_shapes(M, N, K, seed):
     t = inputs.linear_inputs(M, K, N, seed=100 + seed)
     check_linear(t.x, t.w, t.dy)
