@@ -189,7 +189,8 @@ def sample_desc(rows, w_rows):
             f"and the three GEMMs on that sample (float64 numpy oracle), GEMM flops / wall time")
 
 
-REF_SAMPLE = (128, 1024)      # per step of --impl reference (about a second)
+REF_SAMPLE = (128, 1024)      # per step of --impl reference (a second or two), shrunk for long runs
+REF_BUDGET_S = 150.0          # wall-time target of a whole --impl reference run
 CPU_SAMPLE = (256, 8192)  # cpu_baseline of the GPU arm (tens of seconds of CPU work)
 
 
@@ -197,6 +198,13 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     rows, w_rows = REF_SAMPLE
+    # The sampled output features are halved (down to one 128-block) until
+    # all warm-up and timed steps fit in about REF_BUDGET_S seconds at a
+    # conservative per-step estimate.  The metric is flops per second, so the
+    # sample size changes the work per step, not the unit.
+    est = lambda w: 2.5 * w / 1024 + 0.1  # noqa: E731  (seconds per step, 8 host cores)
+    while w_rows > 128 and est(w_rows) * (args.steps + args.warmup) > REF_BUDGET_S:
+        w_rows //= 2
     vals = []
     for _ in range(args.warmup):
         oracle_sample(rows, w_rows)
