@@ -466,9 +466,12 @@ def main():
     ap.add_argument("--no-moe", action="store_true", help="skip the MXFP8 sections (MoE and dense)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
-    world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
+        # Rank 0 alone times the CPU oracle; the other ranks exit without work
+        # (no process group: nothing is exchanged).
+        world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
         return run_reference(args, world, rank)
+    world, rank, local = dist_setup(args.gpus)
     return run_ours(args, world, rank, local)
 
 
