@@ -83,8 +83,8 @@ struct SharedStorageT {
   uint8_t a[S][A_BYTES];  // each stage 1024-byte aligned (swizzle atom)
   uint8_t b[S][B_BYTES];
   uint8_t epi[NUM_EPI_WARPS][EPI];
-  // Per-column B scales of the current and next block, private to each
-  // promotion warp: [warp][buffer][SB_STRIDE * q + 2 * chunk + e] holds column
+  // Per-column B scales of the current and next block (per-column-scale
+  // kernel only), private to each promotion warp: [warp][buffer][SB_STRIDE * q + 2 * chunk + e] holds column
   // 8 * chunk + 2 * q + e (q = lane % 4), so a thread's 32 scales are
   // contiguous and its 16-byte loads of two chunks hit distinct banks.
   float sb_vec[NUM_EPI_WARPS][2][4 * SB_STRIDE];
