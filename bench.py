@@ -436,6 +436,47 @@ def run_moe(dev, steps, warmup, fp8_peak, hbm_peak, world, dense: bool = False):
     }
 
 
+# (M, N, K) rows of the grouped-mm microbenchmark of PR #3037, each at G = 1, 2, 4, 8.
+MOE_TABLE_MNK = [(16384, 8192, 5120), (128000, 8192, 5120), (16384, 1536, 5120), (128000, 1536, 5120),
+                 (16384, 2048, 7168), (128000, 2048, 7168)]
+
+
+def run_moe_table(dev, steps, warmup):
+    """The MXFP8 grouped linear over the shapes of PR #3037's microbenchmark
+    table, in its columns: forward (quantizations + grouped GEMM) and forward
+    + backward (the whole nine-call step) in microseconds.  One JSON line per
+    shape; inputs are seeded N(0,1) / N(0,0.02) / N(0,1e-3) draws made on the
+    device (timing only, no parity check), token groups of multiples of 32."""
+    import torch
+
+    from mxfp8_precision_gemms_fp8bw_gb300 import binding as B
+    from mxfp8_precision_gemms_fp8bw_gb300 import inputs
+    from mxfp8_precision_gemms_fp8bw_gb300.linear import MxMoEWorkspace
+
+    for (M, N, K) in MOE_TABLE_MNK:
+        for G in (1, 2, 4, 8):
+            g = torch.Generator(device=dev)
+            g.manual_seed(1000 * G + M % 1000 + N + K)
+            draw = lambda shape, std: (torch.randn(shape, generator=g, device=dev) * std).bfloat16()  # noqa: E731
+            x, w, dy = draw((M, K), 1.0), draw((G, N, K), 0.02), draw((M, N), 1e-3)
+            sizes = inputs.moe_group_sizes(np.random.default_rng(G), M, G)
+            ge = torch.from_numpy(np.cumsum(sizes).astype(np.int32)).to(dev)
+            ws = MxMoEWorkspace(M, N, K, G, device=dev)
+            kern = ws.kernels(x, w, dy, ge)
+            for _ in range(warmup):
+                ws.step(x, w, dy, ge)
+            B.fp8bw_sync_status()
+            ms, per = time_kernels(kern, steps, torch.cuda.current_stream(dev))
+            B.fp8bw_sync_status()
+            lu = linear_us(per, ["mx_quant_1x32_row(x)", "mx_quant_1x32_row(W)", "mx_grouped_fwd"])
+            print(json.dumps({"table": "mxfp8_grouped_mm", "M": M, "N": N, "K": K, "G": G, **lu,
+                              "fwd_bwd_tflops": round(6 * M * N * K / (lu["fwd_bwd_us"] * 1e-6) / 1e12, 1)}),
+                  flush=True)
+            del x, w, dy, ws, kern
+            torch.cuda.empty_cache()
+    return 0
+
+
 def load_traffic(kernel: str):
     """DRAM bytes (read + write) per launch of `kernel` from the committed ncu
     summary, if the kernel's sources still hash to what was profiled; else None."""
@@ -464,6 +505,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-moe", action="store_true", help="skip the MXFP8 sections (MoE and dense)")
+    ap.add_argument("--moe-table", action="store_true",
+                    help="instead of the bench line, time the MXFP8 grouped linear over the shapes of the "
+                         "grouped-mm microbenchmark table (one JSON line per shape)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     if args.impl == "reference":
@@ -472,6 +516,12 @@ def main():
         world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
         return run_reference(args, world, rank)
     world, rank, local = dist_setup(args.gpus)
+    if args.moe_table:
+        import torch
+        torch.cuda.set_device(local)
+        from mxfp8_precision_gemms_fp8bw_gb300 import binding as B
+        B.lib(build_if_missing=True)
+        return run_moe_table(torch.device("cuda", local), min(args.steps, 20), args.warmup)
     return run_ours(args, world, rank, local)
 
 
