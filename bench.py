@@ -441,6 +441,44 @@ MOE_TABLE_MNK = [(16384, 8192, 5120), (128000, 8192, 5120), (16384, 1536, 5120),
                  (16384, 2048, 7168), (128000, 2048, 7168)]
 
 
+# (M, K, N) of the blockwise linear workloads: the dense one and the two large-token ones.
+DENSE_TABLE_MKN = [(16384, 5120, 8192), (128000, 7168, 2048), (128000, 5120, 1536)]
+
+
+def run_dense_table(dev, steps, warmup):
+    """The blockwise-FP8 linear (six calls) over the dense and large-token
+    workload shapes: per-kernel microseconds, forward (x and W quantization +
+    fwd GEMM) and forward+backward microseconds, GEMM TFLOP/s.  One JSON line
+    per shape; seeded device-side draws, timing only."""
+    import torch
+
+    from mxfp8_precision_gemms_fp8bw_gb300 import binding as B
+    from mxfp8_precision_gemms_fp8bw_gb300.linear import BlockwiseLinearWorkspace
+
+    for (M, K, N) in DENSE_TABLE_MKN:
+        g = torch.Generator(device=dev)
+        g.manual_seed(M + K + N)
+        draw = lambda shape, std: (torch.randn(shape, generator=g, device=dev) * std).bfloat16()  # noqa: E731
+        x, w, dy = draw((M, K), 1.0), draw((N, K), 0.02), draw((M, N), 1e-3)
+        ws = BlockwiseLinearWorkspace(M, N, K, device=dev)
+        kern = ws.kernels(x, w, dy)
+        for _ in range(warmup):
+            ws.step(x, w, dy)
+        B.fp8bw_sync_status()
+        ms, per = time_kernels(kern, steps, torch.cuda.current_stream(dev))
+        B.fp8bw_sync_status()
+        lu = linear_us(per, ["quant_1x128_rowcol(x)", "quant_128x128(W)", "gemm_fwd"])
+        gemm_ms = sum(v for n, v in per.items() if n.startswith("gemm"))
+        print(json.dumps({"table": "blockwise_linear", "M": M, "K": K, "N": N, **lu,
+                          "kernels_us": {n: round(v * 1e3, 1) for n, v in per.items()},
+                          "gemm_tflops": round(6 * M * N * K / (gemm_ms * 1e-3) / 1e12, 1),
+                          "fwd_bwd_tflops": round(6 * M * N * K / (lu["fwd_bwd_us"] * 1e-6) / 1e12, 1)}),
+              flush=True)
+        del x, w, dy, ws, kern
+        torch.cuda.empty_cache()
+    return 0
+
+
 def run_moe_table(dev, steps, warmup):
     """The MXFP8 grouped linear over the shapes of PR #3037's microbenchmark
     table, in its columns: forward (quantizations + grouped GEMM) and forward
@@ -506,8 +544,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-moe", action="store_true", help="skip the MXFP8 sections (MoE and dense)")
     ap.add_argument("--moe-table", action="store_true",
-                    help="instead of the bench line, time the MXFP8 grouped linear over the shapes of the "
-                         "grouped-mm microbenchmark table (one JSON line per shape)")
+                    help="instead of the bench line, time the blockwise linear over the dense and large-token "
+                         "shapes and the MXFP8 grouped linear over the shapes of the grouped-mm microbenchmark "
+                         "table (one JSON line per shape)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     if args.impl == "reference":
@@ -521,7 +560,9 @@ def main():
         torch.cuda.set_device(local)
         from mxfp8_precision_gemms_fp8bw_gb300 import binding as B
         B.lib(build_if_missing=True)
-        return run_moe_table(torch.device("cuda", local), min(args.steps, 20), args.warmup)
+        dev = torch.device("cuda", local)
+        run_dense_table(dev, min(args.steps, 20), args.warmup)
+        return run_moe_table(dev, min(args.steps, 20), args.warmup)
     return run_ours(args, world, rank, local)
 
 
