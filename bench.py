@@ -543,7 +543,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-moe", action="store_true", help="skip the MXFP8 sections (MoE and dense)")
-    ap.add_argument("--moe-table", action="store_true",
+    ap.add_argument("--tables", action="store_true",
                     help="instead of the bench line, time the blockwise linear over the dense and large-token "
                          "shapes and the MXFP8 grouped linear over the shapes of the grouped-mm microbenchmark "
                          "table (one JSON line per shape)")
@@ -555,7 +555,7 @@ def main():
         world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
         return run_reference(args, world, rank)
     world, rank, local = dist_setup(args.gpus)
-    if args.moe_table:
+    if args.tables:
         import torch
         torch.cuda.set_device(local)
         from mxfp8_precision_gemms_fp8bw_gb300 import binding as B
