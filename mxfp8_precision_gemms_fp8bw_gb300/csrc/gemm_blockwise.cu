@@ -55,7 +55,12 @@ constexpr int NUM_THREADS = 384;
 constexpr int EPI_WARP0 = 4;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;  // two BN-column fp32 partial buffers
-constexpr int GROUP_M = 16;          // tile raster: 16 row-blocks share a column sweep
+// Tile raster: group_m() row-blocks share a column sweep (one B scale per
+// block: 32; per-column B scale: 16, each measured fastest).
+template <int kBScale>
+__host__ __device__ constexpr int group_m() {
+  return kBScale == 0 ? 32 : 16;
+}
 constexpr int SB_STRIDE = 36;        // floats per lane-quarter row of the staged column scales
 constexpr int EPI_BOX_ROWS = 16;     // output staging box: 16 rows x 64 bf16 columns (128 B rows)
 constexpr int EPI_BOX_COLS = 64;
@@ -116,11 +121,12 @@ __device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, ui
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+template <int kGroupM>
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
-  const int group_size = GROUP_M * num_n;
+  const int group_size = kGroupM * num_n;
   const int g = tile / group_size;
-  const int first_m = g * GROUP_M;
-  const int gm = min(num_m - first_m, GROUP_M);
+  const int first_m = g * kGroupM;
+  const int gm = min(num_m - first_m, kGroupM);
   const int t = tile - g * group_size;
   mb = first_m + t % gm;
   nb = t / gm;
@@ -198,7 +204,7 @@ __device__ __forceinline__ void promote_per_column(SharedStorageT<1>& sm, uint32
   bool alive = true;
   for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
     int mb, nb;
-    tile_coords(tile, num_m, num_n, mb, nb);
+    tile_coords<group_m<1>()>(tile, num_m, num_n, mb, nb);
     const int64_t rbase = static_cast<int64_t>(mb) * BM + quarter * 32 + r8;  // rows rbase + 16h + 8e
     const int64_t col0 = static_cast<int64_t>(nb) * BN + half * 128;
     float2 acc[64];  // column pair 2*q4 of chunk k, row 16h + 8e: acc[(h * 16 + k) * 2 + e]
@@ -375,7 +381,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool alive = true;
       for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
         int mb, nb;
-        tile_coords(tile, num_m, num_n, mb, nb);
+        tile_coords<group_m<kBScale>()>(tile, num_m, num_n, mb, nb);
         for (int kb = 0; kb < num_k; ++kb) {
           if (!mbar_wait(&sm.empty[stage], phase ^ 1u, ab, status)) {
             alive = false;
@@ -468,7 +474,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool alive = true;
       for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
         int mb, nb;
-        tile_coords(tile, num_m, num_n, mb, nb);
+        tile_coords<group_m<kBScale>()>(tile, num_m, num_n, mb, nb);
         const int64_t m = static_cast<int64_t>(mb) * BM + row;
         const int64_t col0 = static_cast<int64_t>(nb) * BN + half * 128;
         float2 acc[64];
