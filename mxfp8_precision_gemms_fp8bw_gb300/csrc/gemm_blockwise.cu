@@ -150,13 +150,6 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int k) {
   return static_cast<uint32_t>(r * 128 + ((k ^ (r & 7)) << 4));
 }
 
-__device__ __forceinline__ void st_global_v8(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
-                                             uint32_t f, uint32_t g, uint32_t h) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d),
-               "r"(e), "r"(f), "r"(g), "r"(h)
-               : "memory");
-}
-
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
