@@ -96,6 +96,23 @@ def test_grouped_small(M, K, N, group_end):
     assert max(e) <= TOL, e
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_grouped_random_layouts(seed):
+    # Seeded random expert counts, token splits (multiples of 32, empty groups
+    # allowed) and dims; every group checked against the oracle.
+    rng = np.random.default_rng(2000 + seed)
+    G = int(rng.integers(1, 7))
+    M = 32 * int(rng.integers(4, 65))
+    K = 256 * int(rng.integers(1, 5))
+    N = 256 * int(rng.integers(1, 5))
+    sizes = 32 * rng.multinomial(M // 32, [1.0 / G] * G)
+    ge = np.cumsum(sizes).astype(np.int32)
+    x, w, dy = moe_inputs(M, K, N, ge, seed=3000 + seed)
+    y, dx, dW = gpu_moe(x, w, dy, ge)
+    e = grouped_errors(x, w, dy, ge, y, dx, dW)
+    assert max(e) <= TOL, (G, M, K, N, list(sizes), e)
+
+
 def test_grouped_floor_mode():
     M, K, N, ge = 256, 256, 256, [64, 256]
     x, w, dy = moe_inputs(M, K, N, ge, seed=5)
