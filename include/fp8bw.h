@@ -16,7 +16,10 @@
  * - Every pointer is a DEVICE pointer on the current CUDA device, allocated and
  *   owned by the caller.  The library never allocates device memory, never
  *   frees caller memory and keeps no per-call state (a 4-byte error word per
- *   device is its only global; see fp8bw_sync_status).
+ *   device, see fp8bw_sync_status, and the fixed scratch array of
+ *   mxfp8_grouped_gemm_noalloc are its only globals).  Their device addresses
+ *   are resolved on a device's first call and cached; calls on a device after
+ *   cudaDeviceReset are not supported.
  * - Every pointer must be 16-byte aligned.  Matrices are dense and row-major
  *   with the leading dimension equal to the row length given.
  * - bf16 tensors are passed as raw 16-bit patterns (fp8bw_bf16); e4m3 codes
@@ -235,6 +238,11 @@ size_t mxfp8_grouped_gemm_workspace_bytes(int kind, int64_t G, int64_t M, int64_
  * - The first call on a device resolves the array's device address for that
  *   device (with that device current); make that first call before any stream
  *   capture.  No call allocates or frees device memory.
+ * - That address is cached per device for the life of the process.  After
+ *   cudaDeviceReset it no longer names the array (the library's device image
+ *   is loaded again), so do not call the library on a device after resetting
+ *   it; the same holds for every entry point, whose error word address is
+ *   cached the same way.
  * - Every call on a device shares the one array and leaves its contents
  *   behind; each call rewrites all of the scratch it reads, so nothing needs
  *   to start at zero.  Calls whose executions overlap on the GPU (different
