@@ -237,37 +237,56 @@ __device__ __forceinline__ void promote_per_column(SharedStorageT<1>& sm, uint32
       tc_fence_after();
       const uint32_t t_col = tmem + static_cast<uint32_t>(buf * BN + half * 128);
       const uint32_t sbv = smem_u32(sm.sb_vec[ew][kb & 1] + q4 * SB_STRIDE);
-      // Eight load/wait rounds of 16 lanes x 32 columns: column quarter cq
-      // of the warp's 128 columns, lane half h of its 32 TMEM lanes.  The
-      // scales of a column quarter (chunks 4cq .. 4cq + 3) serve both halves.
+      // Load/wait rounds over the warp's 128 columns: each round takes kCqr
+      // column quarters (chunks 4cq .. 4cq + 3) for both 16-lane halves h of
+      // the warp's 32 TMEM lanes, then one wait.  The scales of a column
+      // quarter serve both halves.
+      // One column quarter per round: wider rounds (more loads before a wait)
+      // measured no faster, the partial's TMEM reads being what sets the pace.
+      constexpr int kCqr = 1;
 #pragma unroll
-      for (int cq = 0; cq < 4; ++cq) {
-        const float4 s01 = lds_f32x4(sbv + 32 * cq);       // chunks 4cq, 4cq + 1
-        const float4 s23 = lds_f32x4(sbv + 32 * cq + 16);  // chunks 4cq + 2, 4cq + 3
-        const float2 sc[4] = {make_float2(s01.x, s01.y), make_float2(s01.z, s01.w), make_float2(s23.x, s23.y),
-                              make_float2(s23.z, s23.w)};
+      for (int rr = 0; rr < 4 / kCqr; ++rr) {
+        float2 sc[kCqr][4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t r[16];
-          tmem_ld_16x256b_x4(t_col + (static_cast<uint32_t>(quarter * 32 + 16 * h) << 16) + cq * 32, r);
-          tmem_ld_wait();
-          if (cq == 3 && h == 1) {
-            // The whole partial is in registers: the buffer goes back to the MMA warp.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
-          }
-          const float2 fa0 = make_float2(sa_cur[h * 2], sa_cur[h * 2]);
-          const float2 fa1 = make_float2(sa_cur[h * 2 + 1], sa_cur[h * 2 + 1]);
+        for (int c2 = 0; c2 < kCqr; ++c2) {
+          const int cq = rr * kCqr + c2;
+          const float4 s01 = lds_f32x4(sbv + 32 * cq);       // chunks 4cq, 4cq + 1
+          const float4 s23 = lds_f32x4(sbv + 32 * cq + 16);  // chunks 4cq + 2, 4cq + 3
+          sc[c2][0] = make_float2(s01.x, s01.y);
+          sc[c2][1] = make_float2(s01.z, s01.w);
+          sc[c2][2] = make_float2(s23.x, s23.y);
+          sc[c2][3] = make_float2(s23.z, s23.w);
+        }
+        uint32_t r[kCqr][2][16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int k = cq * 4 + c;
-            const float2 p0 = make_float2(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]));
-            const float2 p1 = make_float2(__uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
-            float2& a0 = acc[(h * 16 + k) * 2];
-            float2& a1 = acc[(h * 16 + k) * 2 + 1];
-            a0 = __ffma2_rn(__fmul2_rn(p0, sc[c]), fa0, a0);
-            a1 = __ffma2_rn(__fmul2_rn(p1, sc[c]), fa1, a1);
+        for (int c2 = 0; c2 < kCqr; ++c2)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tmem_ld_16x256b_x4(t_col + (static_cast<uint32_t>(quarter * 32 + 16 * h) << 16) + (rr * kCqr + c2) * 32,
+                               r[c2][h]);
+        tmem_ld_wait();
+        if (rr == 4 / kCqr - 1) {
+          // The whole partial is in registers: the buffer goes back to the MMA warp.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
+        }
+#pragma unroll
+        for (int c2 = 0; c2 < kCqr; ++c2) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float2 fa0 = make_float2(sa_cur[h * 2], sa_cur[h * 2]);
+            const float2 fa1 = make_float2(sa_cur[h * 2 + 1], sa_cur[h * 2 + 1]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int k = (rr * kCqr + c2) * 4 + c;
+              const float2 p0 = make_float2(__uint_as_float(r[c2][h][4 * c]), __uint_as_float(r[c2][h][4 * c + 1]));
+              const float2 p1 = make_float2(__uint_as_float(r[c2][h][4 * c + 2]), __uint_as_float(r[c2][h][4 * c + 3]));
+              float2& a0 = acc[(h * 16 + k) * 2];
+              float2& a1 = acc[(h * 16 + k) * 2 + 1];
+              a0 = __ffma2_rn(__fmul2_rn(p0, sc[c2][c]), fa0, a0);
+              a1 = __ffma2_rn(__fmul2_rn(p1, sc[c2][c]), fa1, a1);
+            }
           }
         }
       }
@@ -417,6 +436,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
       const int me = warp - 1;
       const uint32_t d_tmem = tmem + static_cast<uint32_t>(me * BN);
+      // Descriptors of stage 0; stage s and the 32-byte K step k are plain
+      // adds to the start-address field (in 16-byte units).
+      const uint64_t a_desc0 = sdesc_kmajor_sw128(smem_u32(sm.a[0]));
+      const uint64_t b_desc0 = sdesc_kmajor_sw128(smem_u32(sm.b[0]));
       bool alive = true;
       uint32_t g = 0;  // running block index over this CTA's tiles
       for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
@@ -431,13 +454,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sm.a[stage]);
-          const uint32_t b_addr = smem_u32(sm.b[stage]);
-#pragma unroll
-          for (int k = 0; k < BK / 32; ++k) {
-            mma_e4m3(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32), sdesc_kmajor_sw128(b_addr + k * 32), idesc,
-                     k > 0 ? 1u : 0u);
-          }
+          const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage * (A_BYTES >> 4));
+          const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage * (B_BYTES >> 4));
+          mma_e4m3_k<false>(d_tmem, ad, bd, idesc);
+          mma_e4m3_k<true>(d_tmem, ad + 2, bd + 2, idesc);
+          mma_e4m3_k<true>(d_tmem, ad + 4, bd + 4, idesc);
+          mma_e4m3_k<true>(d_tmem, ad + 6, bd + 6, idesc);
           mma_commit(&sm.empty[stage]);
           mma_commit(&sm.tmem_full[me]);
         }
@@ -492,8 +514,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t t_base = tmem + t_lane + static_cast<uint32_t>(buf * BN + half * 128);
           // 16-column TMEM loads, one per wait (eight load/wait rounds per
-          // block measured fastest).  The buffer goes back to the MMA warp as
-          // soon as the last load has landed in registers.
+          // block measured fastest: with 2 or 4 loads per wait the promotion
+          // warps take more of the TMEM read bandwidth the MMAs share and all
+          // three GEMMs slow down by a fifth).  The buffer goes back to the
+          // MMA warp as soon as the last load has landed in registers.
           constexpr int NC = 1;
           constexpr int NG = 8 / NC;
           const float2 f2 = make_float2(sa_cur * sb_cur, sa_cur * sb_cur);

@@ -33,10 +33,15 @@
 // GEMM CTA (persistent, 384 threads):
 //   warp 0      TMA producer: per stage A 128x128 and B 256x128 e4m3 tiles
 //               (tensor maps) plus their 512 B + 1 KB scale chunks (bulk copies)
-//   warp 1      TMEM owner and MMA issuer: tcgen05.cp of the stage's scale
-//               chunks into TMEM, then up to 4 block-scaled MMAs (K = 32 each;
-//               the instruction descriptor selects scale byte j)
-//   warps 2-3   idle
+//   warp 1      TMEM owner and MMA issuer: up to 4 block-scaled MMAs per
+//               stage (K = 32 each; the instruction descriptor selects scale
+//               byte j)
+//   warp 2      scale copier: once a stage has landed, tcgen05.cp of its scale
+//               chunks into that stage's TMEM slot, committed to the stage's
+//               sf_ready barrier, which the MMA issuer waits on instead of the
+//               load barrier (the copies stay off the issuing thread, where
+//               every instruction delays the next MMA)
+//   warp 3      idle
 //   warps 4-11  epilogue: drain the accumulator (warp w: lanes 32*(w%4).., one
 //               128-column half), release it, write bf16 rows.
 #include <mutex>
@@ -121,9 +126,11 @@ struct SharedStorage {
   GroupTable groups;
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
+  uint64_t sf_ready[STAGES];  // the stage's scale factors are in TMEM (and its tiles in smem)
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t mma_drain;
+  uint64_t cp_drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -286,10 +293,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.sf_ready[s], 1);
     }
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.acc_empty, NUM_EPI_WARPS);
     mbar_init(&sm.mma_drain, 1);
+    mbar_init(&sm.cp_drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -358,6 +367,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int stage = 0;
         uint32_t phase = 0, aphase = 0;
         bool alive = true;
+        // Descriptors of stage 0; stage s and the 32-byte K step j are plain
+        // adds to the start-address field (in 16-byte units).
+        const uint64_t a_desc0 = sdesc_kmajor_sw128(smem_u32(sm.a[0]));
+        const uint64_t b_desc0 = sdesc_kmajor_sw128(smem_u32(sm.b[0]));
+        const uint32_t acc = tmem + ACC_COL;
         for (int t = blockIdx.x; t < p.num_tiles && alive; t += gridDim.x) {
           const Tile T = decode(gt, p, t);
           const int nkb = num_kb(T);
@@ -368,23 +382,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           for (int kb = 0; kb < nkb; ++kb) {
-            if (!mbar_wait(&sm.full[stage], phase, ab, status)) {
+            // Waited after the previous stage's last MMA, not before it: the
+            // scale copies that complete sf_ready pass through the tensor
+            // pipe behind the queued MMAs, so an earlier wait stalls the pipe.
+            if (!mbar_wait(&sm.sf_ready[stage], phase, ab, status)) {
               alive = false;
               break;
             }
             tc_fence_after();
             const uint32_t sf_col = tmem + SF_COL0 + static_cast<uint32_t>(stage) * 16;
-            tmem_cp_32x128b_warpx4(sf_col, sdesc_plain_128b_rows(smem_u32(sm.sfa[stage])));
-            tmem_cp_32x128b_warpx4(sf_col + 4, sdesc_plain_128b_rows(smem_u32(sm.sfb[stage])));
-            tmem_cp_32x128b_warpx4(sf_col + 8, sdesc_plain_128b_rows(smem_u32(sm.sfb[stage] + 128)));
             const int k0 = T.k_begin + kb * BK;
             const int chunks = min(4, (T.k_end - k0) / 32);
-            const uint32_t a_addr = smem_u32(sm.a[stage]);
-            const uint32_t b_addr = smem_u32(sm.b[stage]);
-            for (int j = 0; j < chunks; ++j) {
-              mma_mx_e4m3(tmem + ACC_COL, sdesc_kmajor_sw128(a_addr + j * 32), sdesc_kmajor_sw128(b_addr + j * 32),
-                          idesc_mx_e4m3(BM, BN, static_cast<uint32_t>(j), static_cast<uint32_t>(j)), sf_col,
-                          sf_col + 4, (kb > 0 || j > 0) ? 1u : 0u);
+            const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage * (A_BYTES >> 4));
+            const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage * (B_BYTES >> 4));
+            if (chunks == 4) {
+              // A whole 128-deep window: four MMAs, scale byte j for the j-th.
+              if (kb == 0) mma_mx_e4m3_k<false>(acc, ad, bd, idesc_mx_e4m3(BM, BN, 0, 0), sf_col, sf_col + 4);
+              else mma_mx_e4m3_k<true>(acc, ad, bd, idesc_mx_e4m3(BM, BN, 0, 0), sf_col, sf_col + 4);
+              mma_mx_e4m3_k<true>(acc, ad + 2, bd + 2, idesc_mx_e4m3(BM, BN, 1, 1), sf_col, sf_col + 4);
+              mma_mx_e4m3_k<true>(acc, ad + 4, bd + 4, idesc_mx_e4m3(BM, BN, 2, 2), sf_col, sf_col + 4);
+              mma_mx_e4m3_k<true>(acc, ad + 6, bd + 6, idesc_mx_e4m3(BM, BN, 3, 3), sf_col, sf_col + 4);
+            } else {
+              // The last window of a group whose size is not a multiple of 128.
+              for (int j = 0; j < chunks; ++j) {
+                mma_mx_e4m3(acc, ad + 2 * j, bd + 2 * j,
+                            idesc_mx_e4m3(BM, BN, static_cast<uint32_t>(j), static_cast<uint32_t>(j)), sf_col,
+                            sf_col + 4, (kb > 0 || j > 0) ? 1u : 0u);
+              }
             }
             mma_commit(&sm.empty[stage]);
             if (++stage == STAGES) {
@@ -400,6 +424,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mma_commit(&sm.mma_drain);
           int dummy = 0;
           mbar_wait(&sm.mma_drain, 0, AbortFlag{&dummy}, status, 1000000ull);
+        }
+      }
+    } else if (warp == 2) {
+      // ------------------------------------------------------------ scale copier
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        bool alive = true;
+        const uint64_t sfa_desc0 = sdesc_plain_128b_rows(smem_u32(sm.sfa[0]));
+        const uint64_t sfb_desc0 = sdesc_plain_128b_rows(smem_u32(sm.sfb[0]));
+        for (int t = blockIdx.x; t < p.num_tiles && alive; t += gridDim.x) {
+          const int nkb = num_kb(decode(gt, p, t));
+          for (int kb = 0; kb < nkb; ++kb) {
+            // Stage `stage` of this round has landed; its TMEM slot was last
+            // read by the MMAs of the previous round, which completed before
+            // the producer could refill the stage.
+            if (!mbar_wait(&sm.full[stage], phase, ab, status)) {
+              alive = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sf_col = tmem + SF_COL0 + static_cast<uint32_t>(stage) * 16;
+            const uint64_t sfa_d = sfa_desc0 + static_cast<uint64_t>(stage * (SFA_BYTES >> 4));
+            const uint64_t sfb_d = sfb_desc0 + static_cast<uint64_t>(stage * (SFB_BYTES >> 4));
+            tmem_cp_32x128b_warpx4(sf_col, sfa_d);
+            tmem_cp_32x128b_warpx4(sf_col + 4, sfb_d);
+            tmem_cp_32x128b_warpx4(sf_col + 8, sfb_d + ((BM * 4) >> 4));  // B's second 128-row chunk, 512 B on
+            mma_commit(&sm.sf_ready[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if (!alive) {
+          // Unwinding: wait for this thread's copies already issued before TMEM is freed.
+          mma_commit(&sm.cp_drain);
+          int dummy = 0;
+          mbar_wait(&sm.cp_drain, 0, AbortFlag{&dummy}, status, 1000000ull);
         }
       }
     }
