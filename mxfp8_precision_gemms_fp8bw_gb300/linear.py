@@ -333,3 +333,110 @@ class PipelinedLinearSteps:
     def synchronize(self) -> None:
         for st in (self.up, self.comp, self.down):
             st.synchronize()
+
+
+class ToyFFNStep:
+    """Forward+backward of the toy FFN of PR #4295 ("add FSDP and TP tests for
+    Float8BlockwiseLinear", Summary: the ToyModel's w1, w2 and out_proj under
+    the standard FFN plan), out = out_proj(silu(w1 x) * (w2 x)), with every
+    GEMM a blockwise-FP8 library call and every output preallocated.
+
+    Inputs: x [M, dim], w1, w2 [hidden, dim], wo [dim, hidden], dy [M, dim]
+    bf16.  x is quantized once (rowwise and colwise in one pass) for both
+    up-projections.  The silu * mul activation and its derivative are the
+    model's own elementwise code, run as bf16/fp32 torch ops between the
+    library calls (not part of the library).  ``kernels`` lists the step's
+    calls in order as (name, callable) pairs for per-call timing; names of
+    library GEMMs start with "gemm".
+    """
+
+    NAMES = ("quant_1x128_rowcol(x)", "quant_128x128(w1)", "quant_128x128(w2)", "quant_128x128(out_proj)",
+             "gemm_fwd(w1)", "gemm_fwd(w2)", "act silu*mul (torch)", "quant_1x128_rowcol(a)", "gemm_fwd(out_proj)",
+             "quant_1x128_rowcol(dy)", "gemm_dgrad(out_proj)", "gemm_wgrad(out_proj)", "act grad (torch)",
+             "quant_1x128_rowcol(dh1)", "quant_1x128_rowcol(dh2)", "gemm_dgrad(w1)", "gemm_wgrad(w1)",
+             "gemm_dgrad(w2)", "gemm_wgrad(w2)", "dx sum (torch)")
+
+    def __init__(self, M: int, dim: int, hidden: int, device="cuda"):
+        self.M, self.dim, self.hidden = M, dim, hidden
+        u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)  # noqa: E731
+
+        def act(R, C):
+            return {"q": e((R, C), u8), "s": e((C // 128, R), f32), "qT": e((C, R), u8), "sT": e((R // 128, C), f32)}
+
+        def wt(R, C):
+            return QuantizedWeight(e((R, C), u8), e((C, R), u8),
+                                   torch.zeros((R // 128, B.scale_ld_128x128(C)), dtype=f32, device=device))
+
+        self.xa, self.aa, self.dya, self.dh1a, self.dh2a = act(M, dim), act(M, hidden), act(M, dim), \
+            act(M, hidden), act(M, hidden)
+        self.w1q, self.w2q, self.woq = wt(hidden, dim), wt(hidden, dim), wt(dim, hidden)
+        self.h1, self.h2, self.a = e((M, hidden), bf), e((M, hidden), bf), e((M, hidden), bf)
+        self.out, self.da, self.dh1, self.dh2 = e((M, dim), bf), e((M, hidden), bf), e((M, hidden), bf), \
+            e((M, hidden), bf)
+        self.dx1, self.dx2, self.dx = e((M, dim), bf), e((M, dim), bf), e((M, dim), bf)
+        self.d_w1, self.d_w2, self.d_wo = e((hidden, dim), bf), e((hidden, dim), bf), e((dim, hidden), bf)
+
+    @staticmethod
+    def _rowcol(src, a, stream):
+        return lambda: B.fp8bw_quant_1x128_rowcol(src, a["q"], a["s"], a["qT"], a["sT"], stream)
+
+    def _act(self):
+        h1 = self.h1.float()
+        self.a.copy_((h1 * torch.sigmoid(h1) * self.h2.float()).bfloat16())
+
+    def _act_grad(self):
+        h1, h2, da = self.h1.float(), self.h2.float(), self.da.float()
+        sig = torch.sigmoid(h1)
+        self.dh1.copy_((da * h2 * (sig * (1 + h1 * (1 - sig)))).bfloat16())
+        self.dh2.copy_((da * h1 * sig).bfloat16())
+
+    def kernels(self, x, w1, w2, wo, dy, stream=None):
+        xa, aa, dya, d1, d2 = self.xa, self.aa, self.dya, self.dh1a, self.dh2a
+        q1, q2, qo = self.w1q, self.w2q, self.woq
+        return [
+            ("quant_1x128_rowcol(x)", self._rowcol(x, xa, stream)),
+            ("quant_128x128(w1)", lambda: B.fp8bw_quant_128x128(w1, q1.q, q1.qT, q1.s, stream)),
+            ("quant_128x128(w2)", lambda: B.fp8bw_quant_128x128(w2, q2.q, q2.qT, q2.s, stream)),
+            ("quant_128x128(out_proj)", lambda: B.fp8bw_quant_128x128(wo, qo.q, qo.qT, qo.s, stream)),
+            ("gemm_fwd(w1)", lambda: B.fp8bw_gemm_fwd(xa["q"], xa["s"], q1.q, q1.s, self.h1, stream)),
+            ("gemm_fwd(w2)", lambda: B.fp8bw_gemm_fwd(xa["q"], xa["s"], q2.q, q2.s, self.h2, stream)),
+            ("act silu*mul (torch)", self._act),
+            ("quant_1x128_rowcol(a)", self._rowcol(self.a, aa, stream)),
+            ("gemm_fwd(out_proj)", lambda: B.fp8bw_gemm_fwd(aa["q"], aa["s"], qo.q, qo.s, self.out, stream)),
+            ("quant_1x128_rowcol(dy)", self._rowcol(dy, dya, stream)),
+            ("gemm_dgrad(out_proj)", lambda: B.fp8bw_gemm_dgrad(dya["q"], dya["s"], qo.qT, qo.s, self.da, stream)),
+            ("gemm_wgrad(out_proj)",
+             lambda: B.fp8bw_gemm_wgrad(dya["qT"], dya["sT"], aa["qT"], aa["sT"], self.d_wo, stream)),
+            ("act grad (torch)", self._act_grad),
+            ("quant_1x128_rowcol(dh1)", self._rowcol(self.dh1, d1, stream)),
+            ("quant_1x128_rowcol(dh2)", self._rowcol(self.dh2, d2, stream)),
+            ("gemm_dgrad(w1)", lambda: B.fp8bw_gemm_dgrad(d1["q"], d1["s"], q1.qT, q1.s, self.dx1, stream)),
+            ("gemm_wgrad(w1)", lambda: B.fp8bw_gemm_wgrad(d1["qT"], d1["sT"], xa["qT"], xa["sT"], self.d_w1, stream)),
+            ("gemm_dgrad(w2)", lambda: B.fp8bw_gemm_dgrad(d2["q"], d2["s"], q2.qT, q2.s, self.dx2, stream)),
+            ("gemm_wgrad(w2)", lambda: B.fp8bw_gemm_wgrad(d2["qT"], d2["sT"], xa["qT"], xa["sT"], self.d_w2, stream)),
+            ("dx sum (torch)", lambda: torch.add(self.dx1, self.dx2, out=self.dx)),
+        ]
+
+    def step(self, x, w1, w2, wo, dy, stream=None):
+        for _, fn in self.kernels(x, w1, w2, wo, dy, stream):
+            fn()
+        return {"out": self.out, "dx": self.dx, "d_w1": self.d_w1, "d_w2": self.d_w2, "d_out_proj": self.d_wo}
+
+    def algorithmic(self):
+        """Per-call algorithmic work: flops (GEMMs), bytes (quantizers), None (model's torch ops)."""
+        M, D, H = self.M, self.dim, self.hidden
+        rowcol = lambda r, c: r * c * 4 + 2 * 4 * r * c // 128  # noqa: E731
+        w128 = lambda r, c: r * c * 4 + 4 * (r // 128) * (c // 128)  # noqa: E731
+        g = 2 * M * D * H
+        out = {}
+        for n in self.NAMES:
+            if n.startswith("gemm"):
+                out[n] = ("flops", g)
+            elif n.startswith("quant_128x128"):
+                out[n] = ("bytes", w128(D, H))
+            elif n.startswith("quant_1x128_rowcol"):
+                out[n] = ("bytes", rowcol(M, D if n.endswith("(x)") or n.endswith("(dy)") else H))
+            else:
+                out[n] = (None, 0)
+        return out
