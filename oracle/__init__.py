@@ -43,4 +43,5 @@ from .mx import (  # noqa: F401
     mx_quant_1x32_row,
     mx_quant_3d_col,
 )
-from .metrics import GEMM_TOL, SQNR_MIN_DB, normalized_gemm_error, row_norms, sqnr_db  # noqa: F401
+from .metrics import (BF16_ROUNDOFF, FP32_ROUNDOFF, GEMM_TOL, SQNR_MIN_DB, normalized_gemm_error,  # noqa: F401
+                      row_norms, sqnr_db)

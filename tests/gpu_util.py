@@ -66,6 +66,26 @@ def transpose_adversarial(R: int, C: int, seed: int, block: int = 128) -> torch.
     return adversarial_bf16(C, R, seed, block).t().contiguous()
 
 
-def gemm_max_err(c_gpu: np.ndarray, c_ref: np.ndarray, a_deq: np.ndarray, b_deq: np.ndarray) -> float:
-    err = oracle.normalized_gemm_error(c_gpu, c_ref, oracle.row_norms(a_deq), oracle.row_norms(b_deq))
+def gemm_max_err(c_gpu: np.ndarray, c_ref: np.ndarray, a_deq: np.ndarray, b_deq: np.ndarray,
+                 out_roundoff: float = oracle.BF16_ROUNDOFF) -> float:
+    """Largest normalized error (see oracle.normalized_gemm_error) of an output
+    whose format rounds with unit roundoff `out_roundoff` (bf16 unless given)."""
+    err = oracle.normalized_gemm_error(c_gpu, c_ref, oracle.row_norms(a_deq), oracle.row_norms(b_deq), out_roundoff)
     return float(np.max(err))
+
+
+
+def oracle_map(name: str, chunks, **kwargs):
+    """oracle.<name>(*chunk, **kwargs) for every chunk, in a pool of spawned
+    processes (safe after CUDA is initialised in this one; the workers import
+    only numpy and the oracle); returns the results in order."""
+    import concurrent.futures
+    import multiprocessing
+    import os
+
+    import oracle_pool
+
+    workers = max(1, min(len(chunks), (os.cpu_count() or 1)))
+    ctx = multiprocessing.get_context("spawn")
+    with concurrent.futures.ProcessPoolExecutor(max_workers=workers, mp_context=ctx) as ex:
+        return list(ex.map(oracle_pool.call, [(name, c, kwargs) for c in chunks]))

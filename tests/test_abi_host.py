@@ -28,7 +28,7 @@ def test_header_declares_the_abi():
     names = _declared_functions()
     assert names == sorted([
         "fp8bw_quant_1x128_row", "fp8bw_quant_1x128_col", "fp8bw_quant_128x128", "fp8bw_quant_1x128_rowcol",
-        "fp8bw_gemm_fwd", "fp8bw_gemm_dgrad", "fp8bw_gemm_wgrad", "fp8bw_gemm_wgrad_acc_f32",
+        "fp8bw_gemm_fwd", "fp8bw_gemm_fwd_quant", "fp8bw_gemm_dgrad", "fp8bw_gemm_wgrad", "fp8bw_gemm_wgrad_acc_f32",
         "mxfp8_quant_1x32_row", "mxfp8_quant_1x32_col", "mxfp8_quant_3d_col", "mxfp8_grouped_gemm",
         "mxfp8_grouped_gemm_workspace_bytes", "mxfp8_grouped_gemm_noalloc",
         "fp8bw_sync_status", "fp8bw_last_error", "fp8bw_selftest_bounded_wait",
@@ -86,6 +86,18 @@ def test_wgrad_accumulate_validation(L):
     assert L.fp8bw_gemm_wgrad_acc_f32(P, 2 * P, 3 * P, 4 * P, 64 * P + 4, 128, 256, 256, None) == binding.ERR_ALIGN
     # the fp32 output is 4 bytes per element: [N, K] = 256 x 256 from P overlaps the operand at P + 1024
     assert L.fp8bw_gemm_wgrad_acc_f32(P + 1024, 2 * P, 3 * P, 4 * P, P, 128, 256, 256, None) == binding.ERR_LAYOUT
+
+
+def test_fwd_quant_validation(L):
+    ops = (P, 2 * P, 3 * P, 4 * P, 64 * P)                     # xq, xs, wq, ws, y
+    dims = (128, 256, 128, None)                               # M, N, K, stream
+    assert L.fp8bw_gemm_fwd_quant(*ops, None, 80 * P, None, None, *dims) == binding.ERR_NULL
+    assert L.fp8bw_gemm_fwd_quant(*ops, 72 * P, 80 * P, 96 * P, None, *dims) == binding.ERR_NULL   # yqT without ysT
+    assert L.fp8bw_gemm_fwd_quant(*ops, 72 * P + 8, 80 * P, None, None, *dims) == binding.ERR_ALIGN
+    assert L.fp8bw_gemm_fwd_quant(*ops, 72 * P, 80 * P, 96 * P + 4, 104 * P, *dims) == binding.ERR_ALIGN
+    # yq [128, 256] from 64P + 4096 overlaps y [128, 256] bf16 (64 KB from 64P)
+    assert L.fp8bw_gemm_fwd_quant(*ops, 64 * P + 4096, 80 * P, None, None, *dims) == binding.ERR_LAYOUT
+    assert L.fp8bw_gemm_fwd_quant(*ops, 72 * P, 80 * P, None, None, 128, 128, 128, None) == binding.ERR_SHAPE
 
 
 def test_misaligned_pointers_rejected(L):

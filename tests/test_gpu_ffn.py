@@ -3,8 +3,11 @@ out_proj, tokens 4096, dim 2048, hidden 8192, 1 % outlier rows in x) forward
 and backward through Float8BlockwiseLinear GEMMs, and the large-token dense
 workloads (M = 128000) whose wgrad contracts over 128000 tokens.
 
-* GEMMs fed directly by the workload's inputs are checked against the oracle
-  element by element (normalized error <= 2e-3).
+* Every one of the FFN step's nine GEMMs is checked against the oracle element
+  by element (normalized error <= 2e-3), each fed the bf16 tensors the GPU step
+  itself produced (x, a, dy, dh1, dh2 and the weights), quantized by the
+  oracle; the library's quantizations of those intermediates are checked byte
+  for byte.
 * The whole FFN step is run a second time through the oracle (oracle
   quantizers, float64 GEMMs, the same bf16 rounding points and activation):
   the GPU chain must agree with it (SQNR >= 35 dB between the two) and lose
@@ -14,15 +17,15 @@ workloads (M = 128000) whose wgrad contracts over 128000 tokens.
   dx 19.3, d_w1 16.8, d_w2 25.6, d_out_proj 24.8 dB): each 128-token block of
   the colwise (token-blocked) operands holds an outlier row 10-100x larger than
   the rest, which coarsens every other row of the block.  The silu * mul
-  activation between the GEMMs is harness code (bf16 torch ops), as in the
-  ToyModel.
+  activation between the GEMMs is the model's own code (bf16 torch ops), as in
+  the ToyModel.
 """
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from gpu_util import f32, gemm_max_err, lib
+from gpu_util import bits, f32, gemm_max_err, lib, u8
 from mxfp8_precision_gemms_fp8bw_gb300 import inputs
 from mxfp8_precision_gemms_fp8bw_gb300 import linear as L
 
@@ -35,41 +38,64 @@ def _lib():
     lib()
 
 
-def _silu(t):
-    return t * torch.sigmoid(t)
+def _fwd_ref(a, w):
+    """Oracle y = a w^T on bf16-valued float32 inputs, with the dequantized operands."""
+    q, s = oracle.quant_1x128_row(a)
+    wq, _, ws = oracle.quant_128x128(w)
+    ad, wd = oracle.dequant_1x128_row(q, s), oracle.dequant_128x128(wq, ws)
+    return ad @ wd.T, ad, wd
+
+
+def _dgrad_ref(d, w):
+    q, s = oracle.quant_1x128_row(d)
+    wq, _, ws = oracle.quant_128x128(w)
+    dd, wd = oracle.dequant_1x128_row(q, s), oracle.dequant_128x128(wq, ws)
+    return dd @ wd, dd, wd.T
+
+
+def _wgrad_ref(d, a):
+    dq, ds = oracle.quant_1x128_col(d)
+    aq, as_ = oracle.quant_1x128_col(a)
+    dd, ad = oracle.dequant_1x128_row(dq, ds), oracle.dequant_1x128_row(aq, as_)
+    return dd @ ad.T, dd, ad
 
 
 def test_ffn_step_parity_and_sqnr():
     t = inputs.ffn()
-    x, w1, w2, wo, dy = (a.cuda() for a in (t.x, t.w1, t.w2, t.out_proj, t.dy))
-    q1, q2, qo = L.quantize_weight(w1), L.quantize_weight(w2), L.quantize_weight(wo)
-    h1, _ = L.forward(x, q1)
-    h2, _ = L.forward(x, q2)
-    a = (_silu(h1.float()) * h2.float()).bfloat16()
-    out, _ = L.forward(a, qo)
-    da, d_wo = L.backward(dy, a, qo)
-    sig = torch.sigmoid(h1.float())
-    dh1 = (da.float() * h2.float() * (sig * (1 + h1.float() * (1 - sig)))).bfloat16()
-    dh2 = (da.float() * _silu(h1.float())).bfloat16()
-    dx1, d_w1 = L.backward(dh1, x, q1)
-    dx2, d_w2 = L.backward(dh2, x, q2)
-    dx = dx1.float() + dx2.float()
+    x, w1, w2, wo, dy = (v.cuda() for v in (t.x, t.w1, t.w2, t.out_proj, t.dy))
+    M, D = t.x.shape
+    H = t.w1.shape[0]
+    step = L.ToyFFNStep(M, D, H, device=x.device)
+    res = step.step(x, w1, w2, wo, dy)
     torch.cuda.synchronize()
 
-    # Element-wise parity of the GEMMs whose operands are the workload's inputs.
-    xf, w1f, wof, dyf = f32(t.x), f32(t.w1), f32(t.out_proj), f32(t.dy)
-    xq, xs = oracle.quant_1x128_row(xf)
-    xd = oracle.dequant_1x128_row(xq, xs)
-    wq, _, ws = oracle.quant_128x128(w1f)
-    wd = oracle.dequant_128x128(wq, ws)
-    assert gemm_max_err(f32(h1), xd @ wd.T, xd, wd) <= TOL
-    dq, ds = oracle.quant_1x128_row(dyf)
-    dd = oracle.dequant_1x128_row(dq, ds)
-    oq, _, os_ = oracle.quant_128x128(wof)
-    od = oracle.dequant_128x128(oq, os_)
-    assert gemm_max_err(f32(da), dd @ od, dd, od.T) <= TOL
+    xf, w1f, w2f, wof, dyf = (f32(v) for v in (t.x, t.w1, t.w2, t.out_proj, t.dy))
+    af, dh1f, dh2f = f32(step.a), f32(step.dh1), f32(step.dh2)
 
-    gpu = {"out": f32(out), "dx": dx.cpu().numpy(), "d_w1": f32(d_w1), "d_w2": f32(d_w2), "d_out_proj": f32(d_wo)}
+    # The library's quantizations of the step's own intermediates, byte for byte.
+    for src, q in ((af, step.aa), (dh1f, step.dh1a), (dh2f, step.dh2a)):
+        qo, so = oracle.quant_1x128_row(src)
+        assert np.array_equal(u8(q["q"]), qo) and np.array_equal(bits(q["s"]), bits(so))
+        qTo, sTo = oracle.quant_1x128_col(src)
+        assert np.array_equal(u8(q["qT"]), qTo) and np.array_equal(bits(q["sT"]), bits(sTo))
+
+    # All nine GEMMs, element by element, each on the GPU step's own inputs.
+    cases = {
+        "fwd w1 (h1)": (f32(step.h1), _fwd_ref(xf, w1f)),
+        "fwd w2 (h2)": (f32(step.h2), _fwd_ref(xf, w2f)),
+        "fwd out_proj (out)": (f32(step.out), _fwd_ref(af, wof)),
+        "dgrad out_proj (da)": (f32(step.da), _dgrad_ref(dyf, wof)),
+        "wgrad out_proj": (f32(step.d_wo), _wgrad_ref(dyf, af)),
+        "dgrad w1 (dx1)": (f32(step.dx1), _dgrad_ref(dh1f, w1f)),
+        "wgrad w1": (f32(step.d_w1), _wgrad_ref(dh1f, xf)),
+        "dgrad w2 (dx2)": (f32(step.dx2), _dgrad_ref(dh2f, w2f)),
+        "wgrad w2": (f32(step.d_w2), _wgrad_ref(dh2f, xf)),
+    }
+    for name, (got, (ref, an, bn)) in cases.items():
+        assert gemm_max_err(got, ref, an, bn) <= TOL, name
+
+    gpu = {"out": f32(res["out"]), "dx": f32(step.dx1).astype(np.float64) + f32(step.dx2),
+           "d_w1": f32(res["d_w1"]), "d_w2": f32(res["d_w2"]), "d_out_proj": f32(res["d_out_proj"])}
     chain = _oracle_chain(t)
     exact = _unquantized_chain(t)
     for k in gpu:

@@ -1,8 +1,9 @@
 """GPU parity of the three blockwise-scaled GEMMs against the float64 oracle.
 
-Bar: max over elements of |out - ref| / (||a_i|| ||b_j||) <= 2e-3 (the
-oracle's GEMM_TOL; bf16 output rounding alone contributes up to 2^-9), and
-end-to-end SQNR >= 25 dB against the product of the unquantized bf16 inputs.
+Bar: max over elements of (|out - ref| - 2^-8 |ref|) / (||a_i|| ||b_j||) <=
+2e-3 (the oracle's GEMM_TOL, with the bf16 output's own rounding, up to
+2^-8 |ref|, allowed on top), and end-to-end SQNR >= 25 dB against the product
+of the unquantized bf16 inputs.
 Shapes span one tile, several tiles with more tiles than SMs, an odd number
 of contraction blocks (wgrad over M = 384) with more tiles than SMs, the tiny
 workload, and the full-size dense workload on sampled output rows.

@@ -2,15 +2,17 @@
 
 Covers several tiles with ragged edges (MX), the edge cases of
 ``gpu_util.adversarial_bf16``, both MX exponent modes, and the full-size dense
-linear workload (x[16384, 5120], W[8192, 5120], dy[16384, 8192]) compared in
-row chunks.
+linear workload (x[16384, 5120], W[8192, 5120], dy[16384, 8192]) and the
+full-size MXFP8 MoE tensors (x[16384, 5120], dy[16384, 8192] rowwise and
+colwise, the expert weights W[8, 8192, 5120] rowwise and 3D colwise),
+compared byte for byte in row chunks.
 """
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from gpu_util import adversarial_bf16, bits, dense_inputs, f32, lib, transpose_adversarial, u8
+from gpu_util import adversarial_bf16, bits, dense_inputs, f32, lib, oracle_map, transpose_adversarial, u8
 from mxfp8_precision_gemms_fp8bw_gb300 import binding as B
 from mxfp8_precision_gemms_fp8bw_gb300 import inputs
 
@@ -188,6 +190,57 @@ def test_full_size_dense_weight_quant(dense):
         assert np.array_equal(q[r0:r1], qo)
         assert np.array_equal(qT[:, r0:r1], qTo)
         assert np.array_equal(bits(s[r0 // 128:r1 // 128, :so.shape[1]]), bits(so))
+
+
+@pytest.fixture(scope="module")
+def moe_tensors():
+    return inputs.moe()
+
+
+def _mx_gpu(kind, t):
+    """One MX quantization of the bf16 tensor t on the GPU: kind row, col or 3d."""
+    td = t.cuda()
+    if kind == "row":
+        q, e = B.alloc_mx_row(td)
+        B.mxfp8_quant_1x32_row(td, q, e)
+    elif kind == "col":
+        q, e = B.alloc_mx_col(td)
+        B.mxfp8_quant_1x32_col(td, q, e)
+    else:
+        q, e = B.alloc_mx_3d_col(td)
+        B.mxfp8_quant_3d_col(td, q, e)
+    B.fp8bw_sync_status()
+    return u8(q), u8(e)
+
+
+@pytest.mark.parametrize("name", ["x", "dy", "w"])
+def test_full_size_moe_mx_quant_bit_exact(moe_tensors, name):
+    # Every byte of the full-size MoE tensors' MX quantizations against the
+    # oracle: rowwise (1x32 along the last dim) for x, dy and W viewed as
+    # [G*N, K]; colwise (32 rows, written transposed) for x and dy; 3D colwise
+    # (32 along N per expert, written [G, K, N]) for W.  Both sides in RCEIL.
+    t = getattr(moe_tensors, name)
+    R2 = t.reshape(-1, t.shape[-1])
+    q, e = _mx_gpu("row", R2)
+    host = f32(R2)
+    chunks = [(np.ascontiguousarray(host[r0:r1]),) for r0, r1 in _chunks(host.shape[0], 2048)]
+    for (r0, r1), (qo, eo) in zip(_chunks(host.shape[0], 2048), oracle_map("mx_quant_1x32_row", chunks)):
+        assert np.array_equal(q[r0:r1], qo), (name, "row", r0)
+        assert np.array_equal(e[r0:r1], eo), (name, "row e8", r0)
+    if name != "w":
+        qT, eT = _mx_gpu("col", t)
+        for (r0, r1), (qo, eo) in zip(_chunks(host.shape[0], 2048), oracle_map("mx_quant_1x32_col", chunks)):
+            assert np.array_equal(qT[:, r0:r1], qo), (name, "col", r0)
+            assert np.array_equal(eT[:, r0 // 32:r1 // 32], eo), (name, "col e8", r0)
+    else:
+        G, N, K = t.shape
+        qT, eT = _mx_gpu("3d", t)
+        h3 = host.reshape(G, N, K)
+        spans = [(g, n0, n1) for g in range(G) for n0, n1 in _chunks(N, 2048)]
+        results = oracle_map("mx_quant_1x32_col", [(np.ascontiguousarray(h3[g, n0:n1]),) for g, n0, n1 in spans])
+        for (g, n0, n1), (qo, eo) in zip(spans, results):
+            assert np.array_equal(qT[g][:, n0:n1], qo), ("w", "3d", g, n0)
+            assert np.array_equal(eT[g][:, n0 // 32:n1 // 32], eo), ("w", "3d e8", g, n0)
 
 
 def test_selftest_bounded_wait_reports_timeout():

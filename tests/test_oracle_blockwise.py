@@ -242,7 +242,29 @@ def test_metrics_closed_forms():
     assert oracle.sqnr_db(ref, ref) == float("inf")
     a = np.array([[3.0, 4.0], [0.0, 0.0]])
     assert np.allclose(oracle.row_norms(a), [5.0, 0.0])
-    err = oracle.normalized_gemm_error(np.array([[1.0, 0.0]]), np.array([[0.5, 0.0]]), [2.0], [0.5, 0.0])
+    err = oracle.normalized_gemm_error(np.array([[1.0, 0.0]]), np.array([[0.5, 0.0]]), [2.0], [0.5, 0.0], 0.0)
     assert err[0, 0] == 0.5 and err[0, 1] == 0.0
+    # with the bf16 allowance the first 2^-8 * |ref| of the difference is free
+    err = oracle.normalized_gemm_error(np.array([[1.0]]), np.array([[0.5]]), [2.0], [0.5])
+    assert err[0, 0] == (0.5 - 0.5 / 256) / 1.0
     err2 = oracle.normalized_gemm_error(np.array([[0.0, 1e-9]]), np.zeros((1, 2)), [2.0], [0.5, 0.0])
     assert err2[0, 1] == np.inf
+
+
+def test_bf16_allowance_is_the_format_unit_roundoff():
+    # bf16 has 8 significant bits: next to 64 its spacing is 0.5, so the
+    # correctly rounded bf16 of -67.7497 is -67.5, off by 0.2497 = 0.00369 |C|:
+    # inside 2^-8 |C| (the allowance), beyond 2^-9 |C|.
+    import torch
+    c = -67.74966269465418
+    r = float(torch.tensor(c, dtype=torch.float64).to(torch.bfloat16).to(torch.float64))
+    assert r == -67.5
+    assert 2.0 ** -9 * abs(c) < abs(r - c) <= oracle.BF16_ROUNDOFF * abs(c)
+    # the rounding of every bf16-representable neighbourhood stays within the allowance
+    xs = np.linspace(1.0, 2.0, 100001) * 2.0 ** 5
+    rb = torch.from_numpy(xs).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.all(np.abs(rb - xs) <= oracle.BF16_ROUNDOFF * np.abs(xs))
+    # one bf16 ulp beyond the correctly rounded value is not free: a 2^-7 |C| miss on
+    # parallel operands (|C| = |a||b|) fails the 2e-3 bar
+    assert oracle.normalized_gemm_error(np.array([[c * (1 + 2.0 ** -7)]]), np.array([[c]]), [abs(c)], [1.0])[0, 0] \
+        > oracle.GEMM_TOL

@@ -131,14 +131,23 @@ def test_grouped_fwd_dgrad_brute_force_with_empty_group():
             for n in (0, 17, 63):
                 want = sum(A[m, k] * B[g, n, k] for k in range(K))
                 assert got[m, n] == want
-    # DGRAD: b is [G, K_out, N_contract]
-    a2, ae82, _ = _int_mx(rng, (M, N))
-    b2, be82, _ = _int_mx(rng, (G * K, N))
+    # DGRAD: b is [G, K_out, N_contract].  The whole output is pinned: every
+    # row of every group against an int64 brute force of the group's own
+    # expert (the values are integers times 2^E with E in [-4, 4], so each
+    # operand times 2^4 is an exact integer and the product carries 2^8).
+    a2, ae82, ai2 = _int_mx(rng, (M, N))
+    b2, be82, bi2 = _int_mx(rng, (G * K, N))
     got2 = oracle.mx_grouped_gemm(oracle.KIND_DGRAD, a2, ae82, b2, be82, group_end, G, M, N, K)
     assert got2.shape == (M, K)
-    A2 = _scaled_int(oracle.e4m3_decode(a2), ae82)
-    B2 = _scaled_int(oracle.e4m3_decode(b2), be82).reshape(G, K, N)
-    assert got2[170, 3] == sum(A2[170, n] * B2[3, 3, n] for n in range(N))
+    A2 = ai2 << np.repeat(ae82.astype(np.int64) - 123, 32, axis=-1)
+    B2 = (bi2 << np.repeat(be82.astype(np.int64) - 123, 32, axis=-1)).reshape(G, K, N)
+    want = np.zeros((M, K), np.int64)
+    for g in range(G):
+        for m in range(starts[g], group_end[g]):
+            for k in range(K):
+                want[m, k] = int(np.sum(A2[m] * B2[g, k]))
+    assert np.array_equal(got2 * 256.0, want.astype(np.float64))
+    assert np.count_nonzero(want) > 0.9 * want.size           # the pin is not vacuous
 
 
 def test_grouped_wgrad_sums_to_full_contraction_and_empty_is_zero():
