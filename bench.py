@@ -373,6 +373,7 @@ def run_ours(args, world, rank, local):
     sec_steps = max(10, args.steps // 3)
     large = [run_large_token(dev, i, sec_steps, args.warmup, fp8_peak, peaks["hbm_gbs"], world) for i in (0, 1)]
     ffn = run_ffn(dev, sec_steps, args.warmup, fp8_peak, peaks["hbm_gbs"], world)
+    chain = run_chain_epilogue_quant(dev, sec_steps, args.warmup, fp8_peak, peaks["hbm_gbs"], world)
     moe = None if args.no_moe else run_moe(dev, max(10, args.steps // 3), args.warmup, fp8_peak, peaks["hbm_gbs"],
                                            world)
     mx_dense = None if args.no_moe else run_moe(dev, max(10, args.steps // 3), args.warmup, fp8_peak,
@@ -405,6 +406,7 @@ def run_ours(args, world, rank, local):
             "linear_us": linear_us(per_kernel, ["quant_1x128_rowcol(x)", "quant_128x128(W)", "gemm_fwd"]),
             "large_token": large,
             "toy_ffn": ffn,
+            "linear_chain_epilogue_quant": chain,
             "mxfp8_moe": moe,
             "mxfp8_dense": mx_dense,
         }
@@ -608,6 +610,59 @@ def run_ffn(dev, steps, warmup, fp8_peak, hbm_peak, world):
                               extra={"model_torch_ops_ms": round(torch_ms, 4),
                                      "note": "the activation and its gradient are the model's torch ops, not library "
                                              "calls; the method reaches SQNR 19-26 dB on this outlier workload"})
+
+
+def run_chain_epilogue_quant(dev, steps, warmup, fp8_peak, hbm_peak, world):
+    """Forward of two chained blockwise linears, y2 = (x W1^T) W2^T, at the
+    toy FFN's sizes (tokens 4096, dim 2048, hidden 8192), with the hidden
+    activation y1 quantized (rowwise for the next forward, colwise for its
+    grad_weight) either by the stand-alone fused quantizer or in the epilogue
+    of the GEMM that produces it (fp8bw_gemm_fwd_quant).  Weights are
+    quantized once outside the timed calls."""
+    import torch
+
+    from mxfp8_precision_gemms_fp8bw_gb300 import binding as B
+
+    M_, D_, H_ = 4096, 2048, 8192
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    draw = lambda shape, std: (torch.randn(shape, generator=g, device=dev) * std).bfloat16()  # noqa: E731
+    x, w1, w2 = draw((M_, D_), 1.0), draw((H_, D_), 0.02), draw((D_, H_), 0.02)
+    xq, xs = B.alloc_quant_1x128_row(x)
+    xqT, xsT = B.alloc_quant_1x128_col(x)
+    w1q, _, w1s = B.alloc_quant_128x128(w1, False)
+    w2q, _, w2s = B.alloc_quant_128x128(w2, False)
+    B.fp8bw_quant_128x128(w1, w1q, None, w1s)
+    B.fp8bw_quant_128x128(w2, w2q, None, w2s)
+    y1 = torch.empty((M_, H_), dtype=torch.bfloat16, device=dev)
+    y2 = torch.empty((M_, D_), dtype=torch.bfloat16, device=dev)
+    q1, s1 = B.alloc_quant_1x128_row(y1)
+    q1T, s1T = B.alloc_quant_1x128_col(y1)
+    qx = lambda: B.fp8bw_quant_1x128_rowcol(x, xq, xs, xqT, xsT)  # noqa: E731
+    separate = [("quant_1x128_rowcol(x)", qx),
+                ("gemm_fwd(w1)", lambda: B.fp8bw_gemm_fwd(xq, xs, w1q, w1s, y1)),
+                ("quant_1x128_rowcol(y1)", lambda: B.fp8bw_quant_1x128_rowcol(y1, q1, s1, q1T, s1T)),
+                ("gemm_fwd(w2)", lambda: B.fp8bw_gemm_fwd(q1, s1, w2q, w2s, y2))]
+    fused = [("quant_1x128_rowcol(x)", qx),
+             ("gemm_fwd_quant(w1)", lambda: B.fp8bw_gemm_fwd_quant(xq, xs, w1q, w1s, y1, q1, s1, q1T, s1T)),
+             ("gemm_fwd(w2)", lambda: B.fp8bw_gemm_fwd(q1, s1, w2q, w2s, y2))]
+    out = {"workload": f"two chained blockwise linears, forward, tokens={M_} dim={D_} hidden={H_}, hidden activation "
+                       "quantized rowwise and colwise; device-drawn N(0,1) x, N(0,0.02) weights, seed 1"}
+    for name, kern in (("separate_quantizer", separate), ("epilogue_quantizer", fused)):
+        for _ in range(warmup):
+            for _, fn in kern:
+                fn()
+        B.fp8bw_sync_status()
+        barrier(world)
+        ms, per = time_kernels(kern, steps, torch.cuda.current_stream(dev))
+        B.fp8bw_sync_status()
+        out[name] = {"ms_per_step": round(max_over_ranks(world, ms, dev), 4),
+                     "calls_us": {n: round(v * 1e3, 1) for n, v in per.items()}}
+    out["saved_us"] = round(1e3 * (out["separate_quantizer"]["ms_per_step"] - out["epilogue_quantizer"]["ms_per_step"]),
+                            1)
+    del x, w1, w2, y1, y2
+    torch.cuda.empty_cache()
+    return out
 
 
 # (M, N, K) rows of the grouped-mm microbenchmark of PR #3037, each at G = 1, 2, 4, 8.

@@ -134,6 +134,25 @@ int fp8bw_quant_128x128(const fp8bw_bf16* w, int64_t R, int64_t C,
 int fp8bw_gemm_fwd(const uint8_t* xq, const float* xs, const uint8_t* wq, const float* ws,
                    fp8bw_bf16* y, int64_t M, int64_t N, int64_t K, void* stream);
 
+/* y = x W^T as fp8bw_gemm_fwd, plus, from the same output tiles, the 1x128
+ * rowwise quantization of bf16(y) and optionally its colwise one -- the
+ * quantized operands the next linear's forward and grad_weight GEMMs take,
+ * without reading y back.  Bit-identical to fp8bw_gemm_fwd followed by
+ * fp8bw_quant_1x128_row (or fp8bw_quant_1x128_rowcol) of y.  Each 128 x 256
+ * output tile holds whole 1x128 row blocks and, its 128 rows being one token
+ * block, whole colwise blocks, so the epilogue that writes y quantizes it too.
+ * The pages run every scaling as kernels of their own ([PR2386] "What I saw":
+ * 128x128 scaling of one tensor takes three kernels) and leave performance
+ * work open ("path forward" item 3); this call is such work, not a step the
+ * pages define.
+ *   xq, xs, wq, ws, y : as fp8bw_gemm_fwd
+ *   yq  : e4m3 [M, N]   ys  : fp32 [N/128][M]      (required)
+ *   yqT : e4m3 [N, M]   ysT : fp32 [M/128][N]      (both or neither NULL)
+ * Requires N % 256 == 0. */
+int fp8bw_gemm_fwd_quant(const uint8_t* xq, const float* xs, const uint8_t* wq, const float* ws,
+                         fp8bw_bf16* y, uint8_t* yq, float* ys, uint8_t* yqT, float* ysT,
+                         int64_t M, int64_t N, int64_t K, void* stream);
+
 /* dx = dy W  (dy in 1x128 blocks along N, W in 128x128 blocks).
  *   dyq : e4m3 [M, N]   dys : fp32 [N/128][M]        (fp8bw_quant_1x128_row of dy)
  *   wqT : e4m3 [K, N]   ws  : fp32 [N/128][LD(K)]    (qT and s of fp8bw_quant_128x128 of W)

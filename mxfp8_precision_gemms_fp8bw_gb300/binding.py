@@ -32,6 +32,7 @@ _SIGNATURES = {
     "fp8bw_quant_128x128": [_P, _I64, _I64, _P, _P, _P, _P],
     "fp8bw_quant_1x128_rowcol": [_P, _I64, _I64, _P, _P, _P, _P, _P],
     "fp8bw_gemm_fwd": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
+    "fp8bw_gemm_fwd_quant": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
     "fp8bw_gemm_dgrad": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
     "fp8bw_gemm_wgrad": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
     "fp8bw_gemm_wgrad_acc_f32": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
@@ -161,6 +162,15 @@ def fp8bw_gemm_fwd(xq, xs, wq, ws, y, stream=None) -> None:
     N = wq.shape[0]
     _check(lib().fp8bw_gemm_fwd(_ptr(xq, _U8, "xq"), _ptr(xs, _F32, "xs"), _ptr(wq, _U8, "wq"), _ptr(ws, _F32, "ws"),
                                 _ptr(y, _BF16, "y"), M, N, K, _stream(stream)))
+
+
+def fp8bw_gemm_fwd_quant(xq, xs, wq, ws, y, yq, ys, yqT=None, ysT=None, stream=None) -> None:
+    M, K = xq.shape
+    N = wq.shape[0]
+    _check(lib().fp8bw_gemm_fwd_quant(_ptr(xq, _U8, "xq"), _ptr(xs, _F32, "xs"), _ptr(wq, _U8, "wq"),
+                                      _ptr(ws, _F32, "ws"), _ptr(y, _BF16, "y"), _ptr(yq, _U8, "yq"),
+                                      _ptr(ys, _F32, "ys"), _ptr(yqT, _U8, "yqT"), _ptr(ysT, _F32, "ysT"), M, N, K,
+                                      _stream(stream)))
 
 
 def fp8bw_gemm_dgrad(dyq, dys, wqT, ws, dx, stream=None) -> None:

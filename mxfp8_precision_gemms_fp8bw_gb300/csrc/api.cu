@@ -274,6 +274,43 @@ FP8BW_API int fp8bw_gemm_fwd(const uint8_t* xq, const float* xs, const uint8_t* 
   return gemm_common("fp8bw_gemm_fwd", g, stream);
 }
 
+FP8BW_API int fp8bw_gemm_fwd_quant(const uint8_t* xq, const float* xs, const uint8_t* wq, const float* ws,
+                                   fp8bw_bf16* y, uint8_t* yq, float* ys, uint8_t* yqT, float* ysT, int64_t M,
+                                   int64_t N, int64_t K, void* stream) {
+  const char* name = "fp8bw_gemm_fwd_quant";
+  if (!yq || !ys || (yqT == nullptr) != (ysT == nullptr))
+    return fail(FP8BW_ERR_NULL, "%s: yq and ys must be non-NULL, yqT and ysT both set or both NULL", name);
+  if (!aligned16(yq) || !aligned16(ys) || (yqT && (!aligned16(yqT) || !aligned16(ysT))))
+    return fail(FP8BW_ERR_ALIGN, "%s: pointers must be 16-byte aligned", name);
+  if (dim_ok(M, 128) && dim_ok(N, 256)) {
+    const int64_t n = M * N;
+    if (overlaps(y, n * 2, yq, n) || overlaps(y, n * 2, ys, n / 32) || overlaps(yq, n, ys, n / 32) ||
+        (yqT && (overlaps(y, n * 2, yqT, n) || overlaps(yq, n, yqT, n) || overlaps(y, n * 2, ysT, n / 32) ||
+                 overlaps(yqT, n, ysT, n / 32) || overlaps(ys, n / 32, ysT, n / 32))) ||
+        overlaps(yq, n, xq, M * K) || overlaps(yq, n, wq, N * K) || (yqT && (overlaps(yqT, n, xq, M * K) ||
+                                                                          overlaps(yqT, n, wq, N * K))))
+      return fail(FP8BW_ERR_LAYOUT, "%s: the outputs overlap each other or an operand", name);
+  }
+  fp8bw::BlockwiseGemmArgs g{};
+  g.a = xq;
+  g.b = wq;
+  g.sa = xs;
+  g.sa_ld = M;
+  g.sb = ws;
+  g.sb_ld_nb = FP8BW_SCALE_LD_128X128(K);
+  g.sb_ld_kb = 1;
+  g.b_scale = fp8bw::BScale::kBlock128x128;
+  g.out = y;
+  g.q_out = yq;
+  g.s_out = ys;
+  g.qT_out = yqT;
+  g.sT_out = ysT;
+  g.Mo = M;
+  g.No = N;
+  g.Kc = K;
+  return gemm_common(name, g, stream);
+}
+
 FP8BW_API int fp8bw_gemm_dgrad(const uint8_t* dyq, const float* dys, const uint8_t* wqT, const float* ws,
                                fp8bw_bf16* dx, int64_t M, int64_t N, int64_t K, void* stream) {
   fp8bw::BlockwiseGemmArgs g{};

@@ -42,6 +42,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "quant_math.cuh"
 
 namespace fp8bw {
 namespace {
@@ -98,6 +99,11 @@ struct SharedStorageT {
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t mma_drain[2];       // used only when unwinding after a timeout
+  // Output quantization in the epilogue (one-scale-per-block kernel): per
+  // tile half, the four warps have staged their bf16 rows / have finished
+  // reading the other warps' rows.
+  uint64_t epi_staged[2];
+  uint64_t epi_read[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -338,13 +344,42 @@ __device__ __forceinline__ void promote_per_column(SharedStorageT<1>& sm, uint32
   }
 }
 
-template <int kBScale>
+// Quantized copies of the bf16 output written by the epilogue (see
+// BlockwiseGemmArgs::q_out).
+struct QuantOut {
+  uint8_t* q;
+  float* s;
+  uint8_t* qT;
+  float* sT;
+};
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+// 32 bytes as two 16-byte stores (the caller's arrays are only guaranteed
+// 16-byte alignment).
+__device__ __forceinline__ void stg_2x16(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+               : "memory");
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(static_cast<uint8_t*>(p) + 16), "r"(w[4]),
+               "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// kQuantOut (one-scale-per-block kernel only): 0 = bf16 output alone; 1 = also
+// its 1x128 rowwise quantization; 2 = rowwise and colwise.  Both are the
+// blockwise rule applied to the bf16-rounded output, bit-identical to running
+// the stand-alone quantizers on it.
+template <int kBScale, int kQuantOut>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     blockwise_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                           const __grid_constant__ CUtensorMap tma_out,
                           const float* __restrict__ sa, int64_t sa_ld, const float* __restrict__ sb, int64_t sb_ld_nb,
-                          int64_t sb_ld_kb, uint16_t* __restrict__ out, float* __restrict__ out_acc, int Mo, int No,
-                          int Kc, int* status) {
+                          int64_t sb_ld_kb, uint16_t* __restrict__ out, float* __restrict__ out_acc, QuantOut qo,
+                          int Mo, int No, int Kc, int* status) {
+  static_assert(kQuantOut == 0 || kBScale == 0, "output quantization is implemented for the fwd/dgrad kernel");
   extern __shared__ uint8_t smem_raw[];
   using Storage = SharedStorageT<kBScale>;
   constexpr int STAGES = Storage::S;
@@ -366,6 +401,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     mbar_init(&sm.mma_drain[0], 1);
     mbar_init(&sm.mma_drain[1], 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&sm.epi_staged[h], 4);
+      mbar_init(&sm.epi_read[h], 4);
+    }
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -484,6 +523,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
       const int row = quarter * 32 + lane;       // row of the tile this thread owns
       const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+      uint32_t tile_i = 0;                       // tiles finished by this warp (epilogue barrier phases)
       int buf = 0;
       uint32_t tphase = 0;
       bool alive = true;
@@ -556,6 +596,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // area (two 32 x 64 boxes, 128-byte swizzle) to two TMA stores, which
         // complete while the warp promotes the next tile.
         const uint32_t stage = smem_u32(sm.epi[ew]);
+        if constexpr (kQuantOut == 2) {
+          // The other three warps of this half have read the previous tile's rows.
+          if (tile_i > 0 && !mbar_wait(&sm.epi_read[half], (tile_i - 1) & 1u, ab, status)) break;
+        }
         if (lane == 0) bulk_wait_read_all();  // the previous tile's stores have read the area
         __syncwarp();
 #pragma unroll
@@ -573,6 +617,78 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tma_store_2d(&tma_out, stage + 4096, static_cast<int32_t>(col0) + 64, r0);
           bulk_commit();
         }
+        if constexpr (kQuantOut >= 1) {
+          if constexpr (kQuantOut == 2) {
+            if (lane == 0) mbar_arrive(&sm.epi_staged[half]);  // this warp's rows are staged
+          }
+          // 1x128 rowwise: the thread's row holds the whole block (the warp's
+          // 128 columns of this tile half), in registers.
+          float amax = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const uint32_t pk = pack_bf16x2(acc[j].x, acc[j].y);
+            amax = fmaxf(amax, fmaxf(fabsf(bf16lo_to_f32(pk)), fabsf(bf16hi_to_f32(pk))));
+          }
+          const float sc = blockwise_scale(amax);
+          const float2 s2 = make_float2(sc, sc), ny2 = make_float2(neg_recip(sc), neg_recip(sc));
+          uint8_t* qrow = qo.q + m * No + col0;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int j = c * 16 + i * 2;  // columns 4 (c * 8 + i) .. + 3
+              const uint32_t p0 = pack_bf16x2(acc[j].x, acc[j].y), p1 = pack_bf16x2(acc[j + 1].x, acc[j + 1].y);
+              w[i] = e4m3x4_from_neg(
+                  neg_div_by_scale2(make_float2(bf16lo_to_f32(p0), bf16hi_to_f32(p0)), s2, ny2),
+                  neg_div_by_scale2(make_float2(bf16lo_to_f32(p1), bf16hi_to_f32(p1)), s2, ny2));
+            }
+            stg_2x16(qrow + 32 * c, w);
+          }
+          qo.s[(col0 / 128) * Mo + m] = sc;
+        }
+        if constexpr (kQuantOut == 2) {
+          // 1x128 colwise: the tile's 128 rows are one block of every column.
+          // Thread (quarter q, lane l) takes column 32q + l of this half and
+          // reads its 128 staged values from the four warps' areas (a warp's
+          // 32 lanes read one 64-byte run of a staged row: conflict-free).
+          if (!mbar_wait(&sm.epi_staged[half], tile_i & 1u, ab, status)) break;
+          const int cc = quarter * 32 + lane;
+          const uint32_t col_off = static_cast<uint32_t>((cc >> 6) * 4096 + (cc & 7) * 2);
+          uint32_t v[64];  // rows 2i, 2i + 1 as a bf16 pair
+          float amax = 0.0f;
+#pragma unroll
+          for (int rq = 0; rq < 4; ++rq) {
+            const uint32_t base = smem_u32(sm.epi[half * 4 + rq]) + col_off;
+#pragma unroll
+            for (int r = 0; r < 32; r += 2) {
+              const uint32_t lo = lds_u16(base + sw128_offset(r, (cc & 63) >> 3));
+              const uint32_t hi = lds_u16(base + sw128_offset(r + 1, (cc & 63) >> 3));
+              v[rq * 16 + r / 2] = lo | (hi << 16);
+              amax = fmaxf(amax, fmaxf(fabsf(bf16lo_to_f32(lo)), fabsf(bf16lo_to_f32(hi))));
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.epi_read[half]);  // done with the other warps' rows
+          const float sc = blockwise_scale(amax);
+          const float2 s2 = make_float2(sc, sc), ny2 = make_float2(neg_recip(sc), neg_recip(sc));
+          const int64_t col = col0 + cc;
+          uint8_t* qcol = qo.qT + col * Mo + static_cast<int64_t>(mb) * BM;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int j = c * 16 + i * 2;  // rows 4 (c * 8 + i) .. + 3
+              w[i] = e4m3x4_from_neg(
+                  neg_div_by_scale2(make_float2(bf16lo_to_f32(v[j]), bf16hi_to_f32(v[j])), s2, ny2),
+                  neg_div_by_scale2(make_float2(bf16lo_to_f32(v[j + 1]), bf16hi_to_f32(v[j + 1])), s2, ny2));
+            }
+            stg_2x16(qcol + 32 * c, w);
+          }
+          qo.sT[static_cast<int64_t>(mb) * No + col] = sc;
+        }
+        ++tile_i;
       }
       if (lane == 0) bulk_wait_all();  // this warp's stores are done before the CTA ends
     }
@@ -629,25 +745,19 @@ cudaError_t launch_blockwise_gemm(const BlockwiseGemmArgs& g, cudaStream_t st) {
   if (g.b_scale != BScale::kBlock128x128) to = ta;  // unused by the per-column kernel
   const int num_tiles = static_cast<int>((g.Mo / BM) * (g.No / BN));
   const int grid = num_tiles < g.num_sms ? num_tiles : g.num_sms;
-  cudaError_t e;
-  if (g.b_scale == BScale::kBlock128x128) {
-    e = cudaFuncSetAttribute(blockwise_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem_bytes<0>()));
-    if (e != cudaSuccess) return e;
-    blockwise_gemm_kernel<0><<<grid, NUM_THREADS, smem_bytes<0>(), st>>>(ta, tb, to, g.sa, g.sa_ld, g.sb, g.sb_ld_nb, g.sb_ld_kb,
-                                                                    g.out, g.out_acc, static_cast<int>(g.Mo),
-                                                                    static_cast<int>(g.No), static_cast<int>(g.Kc),
-                                                                    g.status);
-  } else {
-    e = cudaFuncSetAttribute(blockwise_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem_bytes<1>()));
-    if (e != cudaSuccess) return e;
-    blockwise_gemm_kernel<1><<<grid, NUM_THREADS, smem_bytes<1>(), st>>>(ta, tb, to, g.sa, g.sa_ld, g.sb, g.sb_ld_nb, g.sb_ld_kb,
-                                                                    g.out, g.out_acc, static_cast<int>(g.Mo),
-                                                                    static_cast<int>(g.No), static_cast<int>(g.Kc),
-                                                                    g.status);
-  }
-  return cudaGetLastError();
+  const QuantOut qo{g.q_out, g.s_out, g.qT_out, g.sT_out};
+  const int Mo = static_cast<int>(g.Mo), No = static_cast<int>(g.No), Kc = static_cast<int>(g.Kc);
+  auto launch = [&](auto kernel, size_t smem) -> cudaError_t {
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    kernel<<<grid, NUM_THREADS, smem, st>>>(ta, tb, to, g.sa, g.sa_ld, g.sb, g.sb_ld_nb, g.sb_ld_kb, g.out, g.out_acc,
+                                            qo, Mo, No, Kc, g.status);
+    return cudaGetLastError();
+  };
+  if (g.b_scale != BScale::kBlock128x128) return launch(blockwise_gemm_kernel<1, 0>, smem_bytes<1>());
+  if (g.q_out == nullptr) return launch(blockwise_gemm_kernel<0, 0>, smem_bytes<0>());
+  if (g.qT_out == nullptr) return launch(blockwise_gemm_kernel<0, 1>, smem_bytes<0>());
+  return launch(blockwise_gemm_kernel<0, 2>, smem_bytes<0>());
 }
 
 // ---------------------------------------------------------------- bounded-wait self-test

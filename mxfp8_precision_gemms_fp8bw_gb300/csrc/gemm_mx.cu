@@ -474,6 +474,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+    const bool out32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
     uint32_t aphase = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
       const Tile T = decode(gt, p, t);
@@ -513,13 +514,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               v[(g * 4 + c) * 8 + j] = pack_bf16x2(__uint_as_float(r[c][2 * j]), __uint_as_float(r[c][2 * j + 1]));
         }
       }
-      if (store) {
-        // Eight 32-byte stores: each lane writes whole sectors of its row.
+      if (store && out32) {
+        // Eight 32-byte stores: each lane writes whole sectors of its row
+        // (out is 32-byte aligned and every row segment starts a multiple of
+        // 256 bytes into its row).
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(orow + c * 16),
                        "r"(v[8 * c]), "r"(v[8 * c + 1]), "r"(v[8 * c + 2]), "r"(v[8 * c + 3]), "r"(v[8 * c + 4]),
                        "r"(v[8 * c + 5]), "r"(v[8 * c + 6]), "r"(v[8 * c + 7])
+                       : "memory");
+        }
+      } else if (store) {
+        // out only 16-byte aligned: the same bytes as 16-byte stores.
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(orow + c * 8), "r"(v[4 * c]),
+                       "r"(v[4 * c + 1]), "r"(v[4 * c + 2]), "r"(v[4 * c + 3])
                        : "memory");
         }
       }

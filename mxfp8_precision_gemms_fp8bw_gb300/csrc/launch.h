@@ -37,6 +37,13 @@ struct BlockwiseGemmArgs {
   BScale b_scale;
   uint16_t* out;      // [Mo, No] bf16 (unused when out_acc is set)
   float* out_acc;     // kPerRow only, may be null: out_acc[Mo, No] += result in fp32
+  // kBlock128x128 only, may be null: the 1x128 rowwise quantization of the
+  // bf16 output (q_out [Mo, No], s_out [No/128][Mo]) and, with qT_out set
+  // too, its colwise one (qT_out [No, Mo], sT_out [Mo/128][No]).
+  uint8_t* q_out;
+  float* s_out;
+  uint8_t* qT_out;
+  float* sT_out;
   int64_t Mo, No, Kc;
   int* status;
   int num_sms;
