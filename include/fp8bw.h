@@ -110,7 +110,8 @@ int fp8bw_quant_1x128_rowcol(const fp8bw_bf16* x, int64_t R, int64_t C,
  * scaling of one tensor, and "path forward" item 2, a handwritten kernel).
  *   w : bf16 [R, C]   q : e4m3 [R, C]   qT : e4m3 [C, R] or NULL
  *   s : fp32 [R/128][FP8BW_SCALE_LD_128X128(C)] (padding columns untouched)
- * qT, when given, holds the same codes transposed; fp8bw_gemm_dgrad takes it.
+ * qT, when given, holds the same codes transposed; fp8bw_gemm_dgrad can take
+ * it instead of reading q transposed.
  * R and C must be positive multiples of 128. */
 int fp8bw_quant_128x128(const fp8bw_bf16* w, int64_t R, int64_t C,
                         uint8_t* q, uint8_t* qT, float* s, void* stream);
@@ -155,11 +156,16 @@ int fp8bw_gemm_fwd_quant(const uint8_t* xq, const float* xs, const uint8_t* wq, 
 
 /* dx = dy W  (dy in 1x128 blocks along N, W in 128x128 blocks).
  *   dyq : e4m3 [M, N]   dys : fp32 [N/128][M]        (fp8bw_quant_1x128_row of dy)
- *   wqT : e4m3 [K, N]   ws  : fp32 [N/128][LD(K)]    (qT and s of fp8bw_quant_128x128 of W)
+ *   wq  : e4m3 [N, K]   ws  : fp32 [N/128][LD(K)]    (q and s of fp8bw_quant_128x128 of W)
+ *   wqT : e4m3 [K, N] or NULL                         (its qT, optional)
  *   dx  : bf16 [M, K]
+ * The contraction runs over W's rows.  Without wqT the kernel reads W's codes
+ * as stored, contiguous along the output column (the tensor core's transposed
+ * B operand), so the weight quantizer need not write qT; with wqT it reads
+ * the transposed copy.  Both give the same result.  wq must be non-NULL.
  * Requires K % 256 == 0. */
-int fp8bw_gemm_dgrad(const uint8_t* dyq, const float* dys, const uint8_t* wqT, const float* ws,
-                     fp8bw_bf16* dx, int64_t M, int64_t N, int64_t K, void* stream);
+int fp8bw_gemm_dgrad(const uint8_t* dyq, const float* dys, const uint8_t* wq, const uint8_t* wqT,
+                     const float* ws, fp8bw_bf16* dx, int64_t M, int64_t N, int64_t K, void* stream);
 
 /* dW = dy^T x  ("128_1_128_1": both operands in 1x128 blocks along tokens M).
  *   dyqT : e4m3 [N, M]   dysT : fp32 [M/128][N]      (fp8bw_quant_1x128_col of dy)

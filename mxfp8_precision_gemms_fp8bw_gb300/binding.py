@@ -33,7 +33,7 @@ _SIGNATURES = {
     "fp8bw_quant_1x128_rowcol": [_P, _I64, _I64, _P, _P, _P, _P, _P],
     "fp8bw_gemm_fwd": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
     "fp8bw_gemm_fwd_quant": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
-    "fp8bw_gemm_dgrad": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
+    "fp8bw_gemm_dgrad": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
     "fp8bw_gemm_wgrad": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
     "fp8bw_gemm_wgrad_acc_f32": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
     "mxfp8_quant_1x32_row": [_P, _I64, _I64, _P, _P, _INT, _P],
@@ -173,11 +173,13 @@ def fp8bw_gemm_fwd_quant(xq, xs, wq, ws, y, yq, ys, yqT=None, ysT=None, stream=N
                                       _stream(stream)))
 
 
-def fp8bw_gemm_dgrad(dyq, dys, wqT, ws, dx, stream=None) -> None:
+def fp8bw_gemm_dgrad(dyq, dys, wq, wqT, ws, dx, stream=None) -> None:
+    """dx = dy W from W's codes wq [N, K]; wqT [K, N] (its transposed copy) is optional."""
     M, N = dyq.shape
-    K = wqT.shape[0]
-    _check(lib().fp8bw_gemm_dgrad(_ptr(dyq, _U8, "dyq"), _ptr(dys, _F32, "dys"), _ptr(wqT, _U8, "wqT"),
-                                  _ptr(ws, _F32, "ws"), _ptr(dx, _BF16, "dx"), M, N, K, _stream(stream)))
+    K = wq.shape[1]
+    _check(lib().fp8bw_gemm_dgrad(_ptr(dyq, _U8, "dyq"), _ptr(dys, _F32, "dys"), _ptr(wq, _U8, "wq"),
+                                  _ptr(wqT, _U8, "wqT"), _ptr(ws, _F32, "ws"), _ptr(dx, _BF16, "dx"), M, N, K,
+                                  _stream(stream)))
 
 
 def fp8bw_gemm_wgrad(dyqT, dysT, xqT, xsT, dW, stream=None) -> None:

@@ -311,11 +311,16 @@ FP8BW_API int fp8bw_gemm_fwd_quant(const uint8_t* xq, const float* xs, const uin
   return gemm_common(name, g, stream);
 }
 
-FP8BW_API int fp8bw_gemm_dgrad(const uint8_t* dyq, const float* dys, const uint8_t* wqT, const float* ws,
-                               fp8bw_bf16* dx, int64_t M, int64_t N, int64_t K, void* stream) {
+FP8BW_API int fp8bw_gemm_dgrad(const uint8_t* dyq, const float* dys, const uint8_t* wq, const uint8_t* wqT,
+                               const float* ws, fp8bw_bf16* dx, int64_t M, int64_t N, int64_t K, void* stream) {
+  if (!wq) return fail(FP8BW_ERR_NULL, "fp8bw_gemm_dgrad: wq must be non-NULL (wqT is the optional one)");
+  if (wqT && !aligned16(wq)) return fail(FP8BW_ERR_ALIGN, "fp8bw_gemm_dgrad: pointers must be 16-byte aligned");
   fp8bw::BlockwiseGemmArgs g{};
   g.a = dyq;
-  g.b = wqT;
+  // With qT the weight is a K-major operand [K, N]; without it, W's own codes
+  // [N, K] are read MN-major (contiguous along the output column k).
+  g.b = wqT ? wqT : wq;
+  g.b_mn_major = wqT == nullptr;
   g.sa = dys;
   g.sa_ld = M;
   g.sb = ws;

@@ -168,6 +168,22 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory descriptor of an MN-major operand tile (contiguous along
+// M/N) written by TMA with 128-byte swizzling in boxes of 128 contraction rows
+// x 128 bytes of M/N: the swizzle atom is 8 contraction rows x 128 bytes, the
+// 8-row groups of a box are 1024 bytes apart (stride byte offset) and the next
+// 128 bytes of M/N are the next box, box_bytes on (leading byte offset).  A
+// 32-deep contraction step is 32 rows = 4096 bytes further.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t smem_addr, uint32_t box_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);  // start address
+  d |= static_cast<uint64_t>(box_bytes >> 4) << 16;          // leading byte offset: next 128 bytes of M/N
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;               // stride byte offset: next 8 contraction rows
+  d |= static_cast<uint64_t>(1) << 46;                       // descriptor version for tcgen05
+  d |= static_cast<uint64_t>(2) << 61;                       // 128-byte swizzle
+  return d;
+}
+
 // Shared-memory descriptor of an unswizzled array of 8-row x 16-byte core
 // matrices stacked along M/N 128 bytes apart (the source of tcgen05.cp).
 __device__ __forceinline__ uint64_t sdesc_plain_128b_rows(uint32_t smem_addr) {
@@ -187,6 +203,9 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
          | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
+
+// The same with operand B MN-major ("transpose B", bit 16).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32_bmn(int M, int N) { return idesc_e4m3_f32(M, N) | (1u << 16); }
 
 // Instruction descriptor of tcgen05.mma kind::mxf8f6f4.block_scale with e4m3
 // A and B, UE8M0 scale factors, fp32 accumulation, K-major operands; the

@@ -372,7 +372,10 @@ __device__ __forceinline__ void stg_2x16(void* p, const uint32_t (&w)[8]) {
 // its 1x128 rowwise quantization; 2 = rowwise and colwise.  Both are the
 // blockwise rule applied to the bf16-rounded output, bit-identical to running
 // the stand-alone quantizers on it.
-template <int kBScale, int kQuantOut>
+// kBmn (one-scale-per-block kernel only): 1 = operand B is given MN-major,
+// b[k][n] over [Kc, No] (the dgrad weight read from its row-major codes),
+// loaded as two 128-column boxes and fed to the MMA with "transpose B".
+template <int kBScale, int kQuantOut, int kBmn>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     blockwise_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                           const __grid_constant__ CUtensorMap tma_out,
@@ -380,6 +383,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                           int64_t sb_ld_kb, uint16_t* __restrict__ out, float* __restrict__ out_acc, QuantOut qo,
                           int Mo, int No, int Kc, int* status) {
   static_assert(kQuantOut == 0 || kBScale == 0, "output quantization is implemented for the fwd/dgrad kernel");
+  static_assert(kBmn == 0 || kBScale == 0, "an MN-major B is implemented for the fwd/dgrad kernel");
   extern __shared__ uint8_t smem_raw[];
   using Storage = SharedStorageT<kBScale>;
   constexpr int STAGES = Storage::S;
@@ -440,7 +444,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           mbar_arrive_expect_tx(&sm.full[stage], A_BYTES + B_BYTES);
           tma_load_2d(sm.a[stage], &tma_a, &sm.full[stage], kb * BK, mb * BM);
-          tma_load_2d(sm.b[stage], &tma_b, &sm.full[stage], kb * BK, nb * BN);
+          if constexpr (kBmn) {
+            // B[k][n]: two boxes of 128 contraction rows x 128 columns.
+            tma_load_2d(sm.b[stage], &tma_b, &sm.full[stage], nb * BN, kb * BK);
+            tma_load_2d(sm.b[stage] + B_BYTES / 2, &tma_b, &sm.full[stage], nb * BN + 128, kb * BK);
+          } else {
+            tma_load_2d(sm.b[stage], &tma_b, &sm.full[stage], kb * BK, nb * BN);
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -472,13 +482,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // g + 2 go out as soon as the promotion hands buffer g % 2 back, even
     // while the other issuer is still feeding block g + 1 to the tensor core.
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+      constexpr uint32_t idesc = kBmn ? idesc_e4m3_f32_bmn(BM, BN) : idesc_e4m3_f32(BM, BN);
+      // Start-address step of one 32-deep MMA along B: 32 bytes K-major, 32
+      // rows of 128 bytes MN-major (16-byte units).
+      constexpr uint64_t kBStep = kBmn ? (32 * 128) >> 4 : 32 >> 4;
       const int me = warp - 1;
       const uint32_t d_tmem = tmem + static_cast<uint32_t>(me * BN);
       // Descriptors of stage 0; stage s and the 32-byte K step k are plain
       // adds to the start-address field (in 16-byte units).
       const uint64_t a_desc0 = sdesc_kmajor_sw128(smem_u32(sm.a[0]));
-      const uint64_t b_desc0 = sdesc_kmajor_sw128(smem_u32(sm.b[0]));
+      const uint64_t b_desc0 = kBmn ? sdesc_mnmajor_sw128(smem_u32(sm.b[0]), B_BYTES / 2)
+                                    : sdesc_kmajor_sw128(smem_u32(sm.b[0]));
       bool alive = true;
       uint32_t g = 0;  // running block index over this CTA's tiles
       for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
@@ -496,9 +510,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage * (A_BYTES >> 4));
           const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage * (B_BYTES >> 4));
           mma_e4m3_k<false>(d_tmem, ad, bd, idesc);
-          mma_e4m3_k<true>(d_tmem, ad + 2, bd + 2, idesc);
-          mma_e4m3_k<true>(d_tmem, ad + 4, bd + 4, idesc);
-          mma_e4m3_k<true>(d_tmem, ad + 6, bd + 6, idesc);
+          mma_e4m3_k<true>(d_tmem, ad + 2, bd + kBStep, idesc);
+          mma_e4m3_k<true>(d_tmem, ad + 4, bd + 2 * kBStep, idesc);
+          mma_e4m3_k<true>(d_tmem, ad + 6, bd + 3 * kBStep, idesc);
           mma_commit(&sm.empty[stage]);
           mma_commit(&sm.tmem_full[me]);
         }
@@ -739,8 +753,11 @@ bool encode_out_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t c
 
 cudaError_t launch_blockwise_gemm(const BlockwiseGemmArgs& g, cudaStream_t st) {
   CUtensorMap ta, tb, to;
-  if (!encode_kmajor_u8(&ta, g.a, g.Mo, g.Kc, BM) || !encode_kmajor_u8(&tb, g.b, g.No, g.Kc, BN))
-    return cudaErrorInvalidValue;
+  // B K-major: [No, Kc], boxes of BN rows x 128 bytes; MN-major: [Kc, No]
+  // (row length No), boxes of 128 rows x 128 bytes.
+  const bool b_ok = g.b_mn_major ? encode_kmajor_u8(&tb, g.b, g.Kc, g.No, 128)
+                                 : encode_kmajor_u8(&tb, g.b, g.No, g.Kc, BN);
+  if (!encode_kmajor_u8(&ta, g.a, g.Mo, g.Kc, BM) || !b_ok) return cudaErrorInvalidValue;
   if (g.b_scale == BScale::kBlock128x128 && !encode_out_bf16(&to, g.out, g.Mo, g.No)) return cudaErrorInvalidValue;
   if (g.b_scale != BScale::kBlock128x128) to = ta;  // unused by the per-column kernel
   const int num_tiles = static_cast<int>((g.Mo / BM) * (g.No / BN));
@@ -754,10 +771,11 @@ cudaError_t launch_blockwise_gemm(const BlockwiseGemmArgs& g, cudaStream_t st) {
                                             qo, Mo, No, Kc, g.status);
     return cudaGetLastError();
   };
-  if (g.b_scale != BScale::kBlock128x128) return launch(blockwise_gemm_kernel<1, 0>, smem_bytes<1>());
-  if (g.q_out == nullptr) return launch(blockwise_gemm_kernel<0, 0>, smem_bytes<0>());
-  if (g.qT_out == nullptr) return launch(blockwise_gemm_kernel<0, 1>, smem_bytes<0>());
-  return launch(blockwise_gemm_kernel<0, 2>, smem_bytes<0>());
+  if (g.b_scale != BScale::kBlock128x128) return launch(blockwise_gemm_kernel<1, 0, 0>, smem_bytes<1>());
+  if (g.b_mn_major) return launch(blockwise_gemm_kernel<0, 0, 1>, smem_bytes<0>());
+  if (g.q_out == nullptr) return launch(blockwise_gemm_kernel<0, 0, 0>, smem_bytes<0>());
+  if (g.qT_out == nullptr) return launch(blockwise_gemm_kernel<0, 1, 0>, smem_bytes<0>());
+  return launch(blockwise_gemm_kernel<0, 2, 0>, smem_bytes<0>());
 }
 
 // ---------------------------------------------------------------- bounded-wait self-test

@@ -28,7 +28,8 @@ enum class BScale : int {
 
 struct BlockwiseGemmArgs {
   const uint8_t* a;   // [Mo, Kc] e4m3, K-major
-  const uint8_t* b;   // [No, Kc] e4m3, K-major
+  const uint8_t* b;   // [No, Kc] e4m3, K-major, or [Kc, No] when b_mn_major
+  bool b_mn_major;    // kBlock128x128 only, without output quantization
   const float* sa;    // sa[kb * sa_ld + m]
   int64_t sa_ld;
   const float* sb;

@@ -7,11 +7,12 @@ This module only orders the library calls and allocates their outputs with
 torch; every quantization and GEMM runs in libfp8bw's kernels.
 
 Forward   : x -> 1x128 rowwise and colwise in one pass (q_x, s_x, q_x^T, s_x^T);
-            W -> 128x128 (q_W, q_W^T, s_W); y = gemm_fwd(q_x, s_x, q_W, s_W).
+            W -> 128x128 (q_W, s_W); y = gemm_fwd(q_x, s_x, q_W, s_W).
             The colwise x codes (1 byte per element) are kept for backward
             instead of the bf16 x.
 Backward  : dy -> 1x128 rowwise and colwise in one pass;
-            dx = gemm_dgrad(q_dy, s_dy, q_W^T, s_W); dW = gemm_wgrad(q_dy^T, s_dy^T, q_x^T, s_x^T)
+            dx = gemm_dgrad(q_dy, s_dy, q_W, s_W) (W's codes read transposed by the
+            tensor core); dW = gemm_wgrad(q_dy^T, s_dy^T, q_x^T, s_x^T)
 """
 from __future__ import annotations
 
@@ -24,13 +25,15 @@ from . import binding as B
 
 @dataclass
 class QuantizedWeight:
-    q: torch.Tensor    # e4m3 [N, K]
-    qT: torch.Tensor   # e4m3 [K, N]
-    s: torch.Tensor    # fp32 [N/128][LD(K)]
+    q: torch.Tensor                # e4m3 [N, K]
+    qT: torch.Tensor | None        # e4m3 [K, N], the same codes transposed, or None
+    s: torch.Tensor                # fp32 [N/128][LD(K)]
 
 
-def quantize_weight(w: torch.Tensor, stream=None) -> QuantizedWeight:
-    q, qT, s = B.alloc_quant_128x128(w, with_transpose=True)
+def quantize_weight(w: torch.Tensor, stream=None, with_transpose: bool = False) -> QuantizedWeight:
+    """128x128 quantization of W.  dgrad reads q itself (transposed by the
+    tensor core), so the transposed copy is written only when asked for."""
+    q, qT, s = B.alloc_quant_128x128(w, with_transpose=with_transpose)
     B.fp8bw_quant_128x128(w, q, qT, s, stream)
     return QuantizedWeight(q, qT, s)
 
@@ -64,7 +67,7 @@ def backward(dy: torch.Tensor, x_col, wq: QuantizedWeight, stream=None, dW_acc: 
     dyqT, dysT = B.alloc_quant_1x128_col(dy)
     B.fp8bw_quant_1x128_rowcol(dy, dyq, dys, dyqT, dysT, stream)
     dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device)
-    B.fp8bw_gemm_dgrad(dyq, dys, wq.qT, wq.s, dx, stream)
+    B.fp8bw_gemm_dgrad(dyq, dys, wq.q, wq.qT, wq.s, dx, stream)
     if dW_acc is not None:
         B.fp8bw_gemm_wgrad_acc_f32(dyqT, dysT, xqT, xsT, dW_acc, stream)
         return dx, dW_acc
@@ -164,17 +167,19 @@ class BlockwiseLinearWorkspace:
     ``kernels(x, w, dy)`` lists the step's library calls in order as
     (name, callable) pairs, so a caller can time each one; ``step`` runs them.
     Inputs: x [M, K], w [N, K], dy [M, N] bf16 on the workspace's device.
+    With ``weight_transpose`` the weight quantizer also writes q_W^T and dgrad
+    reads that copy instead of q_W.
     """
 
     NAMES = ("quant_1x128_rowcol(x)", "quant_128x128(W)", "gemm_fwd", "quant_1x128_rowcol(dy)", "gemm_dgrad",
              "gemm_wgrad")
 
-    def __init__(self, M: int, N: int, K: int, device="cuda"):
+    def __init__(self, M: int, N: int, K: int, device="cuda", weight_transpose: bool = False):
         self.M, self.N, self.K = M, N, K
         u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
         e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)  # noqa: E731
         self.xq, self.xs = e((M, K), u8), e((K // 128, M), f32)
-        self.wq, self.wqT = e((N, K), u8), e((K, N), u8)
+        self.wq, self.wqT = e((N, K), u8), (e((K, N), u8) if weight_transpose else None)
         self.ws = torch.zeros((N // 128, B.scale_ld_128x128(K)), dtype=f32, device=device)
         self.y = e((M, N), bf)
         self.dyq, self.dys = e((M, N), u8), e((N // 128, M), f32)
@@ -191,7 +196,8 @@ class BlockwiseLinearWorkspace:
             ("gemm_fwd", lambda: B.fp8bw_gemm_fwd(self.xq, self.xs, self.wq, self.ws, self.y, stream)),
             ("quant_1x128_rowcol(dy)",
              lambda: B.fp8bw_quant_1x128_rowcol(dy, self.dyq, self.dys, self.dyqT, self.dysT, stream)),
-            ("gemm_dgrad", lambda: B.fp8bw_gemm_dgrad(self.dyq, self.dys, self.wqT, self.ws, self.dx, stream)),
+            ("gemm_dgrad",
+             lambda: B.fp8bw_gemm_dgrad(self.dyq, self.dys, self.wq, self.wqT, self.ws, self.dx, stream)),
             ("gemm_wgrad", lambda: B.fp8bw_gemm_wgrad(self.dyqT, self.dysT, self.xqT, self.xsT, self.dW, stream)),
         ]
 
@@ -207,7 +213,7 @@ class BlockwiseLinearWorkspace:
         rowcol = lambda r, c: r * c * 4 + 2 * 4 * r * c // 128  # noqa: E731
         return {
             "quant_1x128_rowcol(x)": ("bytes", rowcol(M, K)),
-            "quant_128x128(W)": ("bytes", N * K * 4 + 4 * (N // 128) * (K // 128)),
+            "quant_128x128(W)": ("bytes", N * K * (3 if self.wqT is None else 4) + 4 * (N // 128) * (K // 128)),
             "gemm_fwd": ("flops", 2 * M * N * K),
             "quant_1x128_rowcol(dy)": ("bytes", rowcol(M, N)),
             "gemm_dgrad": ("flops", 2 * M * N * K),
@@ -365,7 +371,7 @@ class ToyFFNStep:
             return {"q": e((R, C), u8), "s": e((C // 128, R), f32), "qT": e((C, R), u8), "sT": e((R // 128, C), f32)}
 
         def wt(R, C):
-            return QuantizedWeight(e((R, C), u8), e((C, R), u8),
+            return QuantizedWeight(e((R, C), u8), None,
                                    torch.zeros((R // 128, B.scale_ld_128x128(C)), dtype=f32, device=device))
 
         self.xa, self.aa, self.dya, self.dh1a, self.dh2a = act(M, dim), act(M, hidden), act(M, dim), \
@@ -405,15 +411,16 @@ class ToyFFNStep:
             ("quant_1x128_rowcol(a)", self._rowcol(self.a, aa, stream)),
             ("gemm_fwd(out_proj)", lambda: B.fp8bw_gemm_fwd(aa["q"], aa["s"], qo.q, qo.s, self.out, stream)),
             ("quant_1x128_rowcol(dy)", self._rowcol(dy, dya, stream)),
-            ("gemm_dgrad(out_proj)", lambda: B.fp8bw_gemm_dgrad(dya["q"], dya["s"], qo.qT, qo.s, self.da, stream)),
+            ("gemm_dgrad(out_proj)",
+             lambda: B.fp8bw_gemm_dgrad(dya["q"], dya["s"], qo.q, qo.qT, qo.s, self.da, stream)),
             ("gemm_wgrad(out_proj)",
              lambda: B.fp8bw_gemm_wgrad(dya["qT"], dya["sT"], aa["qT"], aa["sT"], self.d_wo, stream)),
             ("act grad (torch)", self._act_grad),
             ("quant_1x128_rowcol(dh1)", self._rowcol(self.dh1, d1, stream)),
             ("quant_1x128_rowcol(dh2)", self._rowcol(self.dh2, d2, stream)),
-            ("gemm_dgrad(w1)", lambda: B.fp8bw_gemm_dgrad(d1["q"], d1["s"], q1.qT, q1.s, self.dx1, stream)),
+            ("gemm_dgrad(w1)", lambda: B.fp8bw_gemm_dgrad(d1["q"], d1["s"], q1.q, q1.qT, q1.s, self.dx1, stream)),
             ("gemm_wgrad(w1)", lambda: B.fp8bw_gemm_wgrad(d1["qT"], d1["sT"], xa["qT"], xa["sT"], self.d_w1, stream)),
-            ("gemm_dgrad(w2)", lambda: B.fp8bw_gemm_dgrad(d2["q"], d2["s"], q2.qT, q2.s, self.dx2, stream)),
+            ("gemm_dgrad(w2)", lambda: B.fp8bw_gemm_dgrad(d2["q"], d2["s"], q2.q, q2.qT, q2.s, self.dx2, stream)),
             ("gemm_wgrad(w2)", lambda: B.fp8bw_gemm_wgrad(d2["qT"], d2["sT"], xa["qT"], xa["sT"], self.d_w2, stream)),
             ("dx sum (torch)", lambda: torch.add(self.dx1, self.dx2, out=self.dx)),
         ]
@@ -427,7 +434,7 @@ class ToyFFNStep:
         """Per-call algorithmic work: flops (GEMMs), bytes (quantizers), None (model's torch ops)."""
         M, D, H = self.M, self.dim, self.hidden
         rowcol = lambda r, c: r * c * 4 + 2 * 4 * r * c // 128  # noqa: E731
-        w128 = lambda r, c: r * c * 4 + 4 * (r // 128) * (c // 128)  # noqa: E731
+        w128 = lambda r, c: r * c * 3 + 4 * (r // 128) * (c // 128)  # noqa: E731
         g = 2 * M * D * H
         out = {}
         for n in self.NAMES:

@@ -54,6 +54,13 @@ def test_library_is_sm103a_only_and_self_contained():
 P = 1 << 20  # a fake, 16-byte aligned "device" address; never dereferenced
 
 
+def test_dgrad_needs_wq_and_takes_wqT_optionally(L):
+    # wq is required even when the transposed copy is given; wqT alone is not enough
+    assert L.fp8bw_gemm_dgrad(P, 2 * P, None, 3 * P, 4 * P, 64 * P, 128, 256, 256, None) == binding.ERR_NULL
+    assert L.fp8bw_gemm_dgrad(P, 2 * P, 3 * P, 5 * P + 8, 4 * P, 64 * P, 128, 256, 256, None) == binding.ERR_ALIGN
+    assert L.fp8bw_gemm_dgrad(P, 2 * P, 3 * P + 8, None, 4 * P, 64 * P, 128, 256, 256, None) == binding.ERR_ALIGN
+
+
 def test_null_pointers_rejected(L):
     assert L.fp8bw_quant_1x128_row(None, 128, 128, P, P * 2, None) == binding.ERR_NULL
     assert "non-NULL" in binding.last_error()
@@ -74,7 +81,8 @@ def test_gemm_shapes_rejected(L):
     assert L.fp8bw_gemm_fwd(P, 2 * P, 3 * P, 4 * P, 64 * P, 128, 128, 128, None) == binding.ERR_SHAPE
     assert L.fp8bw_gemm_fwd(P, 2 * P, 3 * P, 4 * P, 64 * P, 96, 256, 128, None) == binding.ERR_SHAPE
     # dgrad: output columns are K
-    assert L.fp8bw_gemm_dgrad(P, 2 * P, 3 * P, 4 * P, 64 * P, 128, 256, 384, None) == binding.ERR_SHAPE
+    assert L.fp8bw_gemm_dgrad(P, 2 * P, 3 * P, None, 4 * P, 64 * P, 128, 256, 384, None) == binding.ERR_SHAPE
+    assert L.fp8bw_gemm_dgrad(P, 2 * P, 3 * P, 5 * P, 4 * P, 64 * P, 128, 256, 384, None) == binding.ERR_SHAPE
     # wgrad: contraction over M must be a multiple of 128
     assert L.fp8bw_gemm_wgrad(P, 2 * P, 3 * P, 4 * P, 64 * P, 64, 256, 256, None) == binding.ERR_SHAPE
 

@@ -151,3 +151,29 @@ def test_float8_blockwise_linear_module_autograd():
     assert gemm_max_err(f32(y), yr, d["x"], d["w"]) <= TOL
     assert gemm_max_err(f32(x.grad), dxr, d["dy"], d["w"].T) <= TOL
     assert gemm_max_err(f32(layer.weight.grad), dWr, d["dyT"], d["xT"]) <= TOL
+
+
+@pytest.mark.parametrize("M,N,K,seed", [(128, 128, 256, 0), (256, 384, 512, 1), (384, 1280, 2304, 2),
+                                        (2048, 4096, 5120, 3)])
+def test_dgrad_from_q_equals_dgrad_from_qT(M, N, K, seed):
+    # dx = dy W computed from W's codes as stored ([N, K], read transposed by
+    # the tensor core) and from the transposed copy ([K, N]): the same products
+    # in the same order, so the same bits; and both within the bar of the oracle.
+    t = inputs.linear_inputs(M, K, N, seed=400 + seed)
+    dyd, wd = t.dy.cuda(), t.w.cuda()
+    wq, wqT, ws = B.alloc_quant_128x128(wd, True)
+    B.fp8bw_quant_128x128(wd, wq, wqT, ws)
+    dyq, dys = B.alloc_quant_1x128_row(dyd)
+    B.fp8bw_quant_1x128_row(dyd, dyq, dys)
+    dx_q = torch.full((M, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dx_qT = torch.full((M, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    B.fp8bw_gemm_dgrad(dyq, dys, wq, None, ws, dx_q)
+    B.fp8bw_gemm_dgrad(dyq, dys, wq, wqT, ws, dx_qT)
+    B.fp8bw_sync_status()
+    assert torch.equal(dx_q, dx_qT)
+    rows = np.arange(M) if M <= 512 else np.sort(np.random.default_rng(seed).choice(M, 256, replace=False))
+    dyf, wf = f32(t.dy[rows]), f32(t.w)
+    oq, os_ = oracle.quant_1x128_row(dyf)
+    woq, _, wos = oracle.quant_128x128(wf)
+    dd, wdq = oracle.dequant_1x128_row(oq, os_), oracle.dequant_128x128(woq, wos)
+    assert gemm_max_err(f32(dx_q)[rows], dd @ wdq, dd, wdq.T) <= TOL

@@ -69,7 +69,7 @@ def test_gemm_outputs_stay_in_bounds(M, N, K):
     B.fp8bw_quant_1x128_col(x, xqT, xsT)
     y, dx, dW = Guarded((M, N), torch.bfloat16), Guarded((M, K), torch.bfloat16), Guarded((N, K), torch.bfloat16)
     B.fp8bw_gemm_fwd(xq, xs, wq, ws, y.t)
-    B.fp8bw_gemm_dgrad(dyq, dys, wqT, ws, dx.t)
+    B.fp8bw_gemm_dgrad(dyq, dys, wq, wqT, ws, dx.t)
     B.fp8bw_gemm_wgrad(dyqT, dysT, xqT, xsT, dW.t)
     B.fp8bw_sync_status()
     assert y.intact() and dx.intact() and dW.intact()
