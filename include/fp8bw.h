@@ -175,6 +175,29 @@ int fp8bw_gemm_dgrad(const uint8_t* dyq, const float* dys, const uint8_t* wq, co
 int fp8bw_gemm_wgrad(const uint8_t* dyqT, const float* dysT, const uint8_t* xqT, const float* xsT,
                      fp8bw_bf16* dW, int64_t M, int64_t N, int64_t K, void* stream);
 
+/* fp8bw_gemm_wgrad with a caller workspace that lets the kernel balance its
+ * last round of output tiles: when the tile count is not a multiple of the
+ * SM count, the remaining tiles are each cut into k contraction parts that
+ * run side by side, and the part that finishes last for a region adds the k
+ * fp32 partials in part order (so the result does not depend on which part
+ * finishes last) and rounds once to bf16.  The result equals
+ * fp8bw_gemm_wgrad's within the GEMM accuracy above; the partials are summed
+ * in a different order, so bits may differ.  (The pages' wgrad runs over the
+ * whole token dimension in one GEMM, [PR2386] "128_1_128_1"; the split is
+ * scheduling work, not a step the pages define.)
+ * workspace: DEVICE memory of at least fp8bw_gemm_wgrad_workspace_bytes(M, N,
+ * K) bytes, 16-byte aligned, owned by the caller; NULL (or a size of 0 from
+ * that query) runs fp8bw_gemm_wgrad unchanged.  Calls that use the same
+ * workspace concurrently race.  Other arguments as fp8bw_gemm_wgrad. */
+int fp8bw_gemm_wgrad_ws(const uint8_t* dyqT, const float* dysT, const uint8_t* xqT, const float* xsT,
+                        fp8bw_bf16* dW, int64_t M, int64_t N, int64_t K, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace fp8bw_gemm_wgrad_ws uses for these dims on the current
+ * device (0 when its tiles fill whole rounds of SMs, or when the dims are
+ * invalid or no device is present).  Enqueues no work. */
+size_t fp8bw_gemm_wgrad_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
 /* dW += dy^T x with dW in fp32: the wgrad GEMM above, its tile added to the
  * caller's fp32 gradient instead of overwriting a bf16 one -- gradient
  * accumulation over micro-batches or token shards, whose sum the optimizer

@@ -36,6 +36,8 @@ _SIGNATURES = {
     "fp8bw_gemm_dgrad": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
     "fp8bw_gemm_wgrad": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
     "fp8bw_gemm_wgrad_acc_f32": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
+    "fp8bw_gemm_wgrad_ws": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, ctypes.c_size_t, _P],
+    "fp8bw_gemm_wgrad_workspace_bytes": [_I64, _I64, _I64],
     "mxfp8_quant_1x32_row": [_P, _I64, _I64, _P, _P, _INT, _P],
     "mxfp8_quant_1x32_col": [_P, _I64, _I64, _P, _P, _INT, _P],
     "mxfp8_quant_3d_col": [_P, _I64, _I64, _I64, _P, _P, _INT, _P],
@@ -72,7 +74,8 @@ def lib(build_if_missing: bool = False) -> ctypes.CDLL:
             fn = getattr(handle, name)
             fn.argtypes = args
             fn.restype = {"fp8bw_last_error": ctypes.c_char_p,
-                          "mxfp8_grouped_gemm_workspace_bytes": ctypes.c_size_t}.get(name, ctypes.c_int)
+                          "mxfp8_grouped_gemm_workspace_bytes": ctypes.c_size_t,
+                          "fp8bw_gemm_wgrad_workspace_bytes": ctypes.c_size_t}.get(name, ctypes.c_int)
         _LIB = handle
     return _LIB
 
@@ -187,6 +190,26 @@ def fp8bw_gemm_wgrad(dyqT, dysT, xqT, xsT, dW, stream=None) -> None:
     K = xqT.shape[0]
     _check(lib().fp8bw_gemm_wgrad(_ptr(dyqT, _U8, "dyqT"), _ptr(dysT, _F32, "dysT"), _ptr(xqT, _U8, "xqT"),
                                   _ptr(xsT, _F32, "xsT"), _ptr(dW, _BF16, "dW"), M, N, K, _stream(stream)))
+
+
+def fp8bw_gemm_wgrad_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().fp8bw_gemm_wgrad_workspace_bytes(M, N, K))
+
+
+def alloc_wgrad_workspace(M: int, N: int, K: int, device) -> torch.Tensor | None:
+    """The workspace fp8bw_gemm_wgrad_ws wants for these dims on this device, or None if it needs none."""
+    n = fp8bw_gemm_wgrad_workspace_bytes(M, N, K)
+    return torch.empty(n, dtype=_U8, device=device) if n else None
+
+
+def fp8bw_gemm_wgrad_ws(dyqT, dysT, xqT, xsT, dW, workspace, stream=None) -> None:
+    N, M = dyqT.shape
+    K = xqT.shape[0]
+    ws = _ptr(workspace, _U8, "workspace") if workspace is not None else None
+    nbytes = workspace.numel() if workspace is not None else 0
+    _check(lib().fp8bw_gemm_wgrad_ws(_ptr(dyqT, _U8, "dyqT"), _ptr(dysT, _F32, "dysT"), _ptr(xqT, _U8, "xqT"),
+                                     _ptr(xsT, _F32, "xsT"), _ptr(dW, _BF16, "dW"), M, N, K, ws, nbytes,
+                                     _stream(stream)))
 
 
 def fp8bw_gemm_wgrad_acc_f32(dyqT, dysT, xqT, xsT, dW, stream=None) -> None:

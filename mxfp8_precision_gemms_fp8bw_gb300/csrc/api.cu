@@ -352,6 +352,52 @@ FP8BW_API int fp8bw_gemm_wgrad(const uint8_t* dyqT, const float* dysT, const uin
   return gemm_common("fp8bw_gemm_wgrad", g, stream);
 }
 
+FP8BW_API size_t fp8bw_gemm_wgrad_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (!dim_ok(M, 128) || !dim_ok(N, 128) || !dim_ok(K, 256)) return 0;
+  int dev = -1, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return fp8bw::wgrad_split_plan(N, K, M, sms).bytes;
+}
+
+FP8BW_API int fp8bw_gemm_wgrad_ws(const uint8_t* dyqT, const float* dysT, const uint8_t* xqT, const float* xsT,
+                                  fp8bw_bf16* dW, int64_t M, int64_t N, int64_t K, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  const char* name = "fp8bw_gemm_wgrad_ws";
+  if (workspace && !aligned16(workspace))
+    return fail(FP8BW_ERR_ALIGN, "%s: the workspace must be 16-byte aligned", name);
+  fp8bw::BlockwiseGemmArgs g{};
+  g.a = dyqT;
+  g.b = xqT;
+  g.sa = dysT;
+  g.sa_ld = N;
+  g.sb = xsT;
+  g.sb_ld_nb = 0;
+  g.sb_ld_kb = K;
+  g.b_scale = fp8bw::BScale::kPerRow;
+  g.out = dW;
+  g.Mo = N;
+  g.No = K;
+  g.Kc = M;
+  if (workspace && dim_ok(M, 128) && dim_ok(N, 128) && dim_ok(K, 256)) {
+    DeviceState* d;
+    if (int rc = current_device(&d)) return rc;
+    const size_t need = fp8bw::wgrad_split_plan(N, K, M, d->num_sms).bytes;
+    if (workspace_bytes < need)
+      return fail(FP8BW_ERR_ARG, "%s: workspace of %zu bytes is smaller than the %zu bytes these dims need", name,
+                  workspace_bytes, need);
+    if (overlaps(workspace, static_cast<int64_t>(need), dW, N * K * 2) ||
+        overlaps(workspace, static_cast<int64_t>(need), dyqT, N * M) ||
+        overlaps(workspace, static_cast<int64_t>(need), xqT, K * M))
+      return fail(FP8BW_ERR_LAYOUT, "%s: the workspace overlaps an operand or the output", name);
+    g.split_ws = workspace;
+    g.split_ws_bytes = workspace_bytes;
+  }
+  return gemm_common(name, g, stream);
+}
+
 FP8BW_API int fp8bw_gemm_wgrad_acc_f32(const uint8_t* dyqT, const float* dysT, const uint8_t* xqT, const float* xsT,
                                        float* dW, int64_t M, int64_t N, int64_t K, void* stream) {
   fp8bw::BlockwiseGemmArgs g{};

@@ -182,6 +182,44 @@ __device__ __forceinline__ void sts_b32(uint32_t addr, uint32_t a) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
 }
 
+// Contraction split of the last round of wgrad tiles.  The first full_units
+// work units are whole tiles; the remaining tiles (when the tile count is not
+// a multiple of the grid) are each cut into k contraction ranges, so the last
+// rounds keep every SM busy.  The part of a split tile that finishes last
+// (per promotion warp, counted in cnt) sums the k fp32 partials in part order
+// from the caller's workspace and writes the output.  k = 1: no split.
+struct SplitK {
+  int full_units;
+  int k;
+  float2* ws;  // [tail tile][part][64][256] float2, thread-major: element j of thread t at j * 256 + t
+  int* cnt;    // [tail tile][8 promotion warps], zero before the launch, back to zero after it
+};
+
+struct Unit {
+  int tile, kb0, kb1;
+  int part;    // -1 for a whole tile
+  int t_idx;   // tail-tile index of a split unit
+};
+
+__device__ __forceinline__ Unit unit_of(int u, const SplitK& sp, int num_k) {
+  Unit U;
+  if (u < sp.full_units) {
+    U.tile = u;
+    U.kb0 = 0;
+    U.kb1 = num_k;
+    U.part = -1;
+    U.t_idx = 0;
+  } else {
+    const int t = u - sp.full_units;
+    U.t_idx = t / sp.k;
+    U.part = t - U.t_idx * sp.k;
+    U.tile = sp.full_units + U.t_idx;
+    U.kb0 = U.part * num_k / sp.k;
+    U.kb1 = (U.part + 1) * num_k / sp.k;
+  }
+  return U;
+}
+
 // Promotion with a per-column B scale (wgrad: both operands in 1x128 blocks
 // along the contraction), out[i, j] = sum_kb sa[kb][i] * sb[kb][j] * P_kb[i, j].
 // Every column of a block has its own scale, which every row needs.  Reading
@@ -191,19 +229,21 @@ __device__ __forceinline__ void sts_b32(uint32_t addr, uint32_t a) {
 // contiguous: one conflict-free 16-byte shared load covers two chunks for
 // both lane halves (8 loads per thread per block).  Shared-memory loads
 // compete with the tensor core's operand reads, so they are kept this few.
+template <bool kSplit>
 __device__ __forceinline__ void promote_per_column(SharedStorageT<1>& sm, uint32_t tmem, int ew, int half, int quarter,
-                                                   int lane, int num_tiles, int num_m, int num_n, int num_k,
+                                                   int lane, int num_units, int num_m, int num_n, int num_k,
                                                    const float* __restrict__ sa, int64_t sa_ld,
                                                    const float* __restrict__ sb, int64_t sb_ld_kb,
                                                    uint16_t* __restrict__ out, float* __restrict__ out_acc, int No,
-                                                   int* status, AbortFlag ab) {
+                                                   const SplitK& sp, int* status, AbortFlag ab) {
   const int q4 = lane & 3, r8 = lane >> 2;
   int buf = 0;
   uint32_t tphase = 0;
   bool alive = true;
-  for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
+  for (int u = blockIdx.x; u < num_units && alive; u += gridDim.x) {
+    const Unit U = kSplit ? unit_of(u, sp, num_k) : Unit{u, 0, num_k, -1, 0};
     int mb, nb;
-    tile_coords<group_m<1>()>(tile, num_m, num_n, mb, nb);
+    tile_coords<group_m<1>()>(U.tile, num_m, num_n, mb, nb);
     const int64_t rbase = static_cast<int64_t>(mb) * BM + quarter * 32 + r8;  // rows rbase + 16h + 8e
     const int64_t col0 = static_cast<int64_t>(nb) * BN + half * 128;
     float2 acc[64];  // column pair 2*q4 of chunk k, row 16h + 8e: acc[(h * 16 + k) * 2 + e]
@@ -215,9 +255,9 @@ __device__ __forceinline__ void promote_per_column(SharedStorageT<1>& sm, uint32
     // row per warp) and stages them in the warp's own shared buffer, and the
     // A scale of one of the warp's 32 rows, which shuffles hand to the four
     // threads holding that row (one global load per lane instead of four).
-    float sa_lane = __ldg(sa + (rbase - r8) + lane);
-    float4 sb4_next = __ldg(reinterpret_cast<const float4*>(sb + col0) + lane);
-    for (int kb = 0; kb < num_k; ++kb) {
+    float sa_lane = __ldg(sa + static_cast<int64_t>(U.kb0) * sa_ld + (rbase - r8) + lane);
+    float4 sb4_next = __ldg(reinterpret_cast<const float4*>(sb + static_cast<int64_t>(U.kb0) * sb_ld_kb + col0) + lane);
+    for (int kb = U.kb0; kb < U.kb1; ++kb) {
       float sa_cur[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) sa_cur[i] = __shfl_sync(0xffffffffu, sa_lane, r8 + 16 * (i >> 1) + 8 * (i & 1));
@@ -231,7 +271,7 @@ __device__ __forceinline__ void promote_per_column(SharedStorageT<1>& sm, uint32
         sts_f32x2(dst + SB_STRIDE * 4, sb4_next.z, sb4_next.w);
       }
       __syncwarp();
-      if (kb + 1 < num_k) {
+      if (kb + 1 < U.kb1) {
         const float* sak = sa + static_cast<int64_t>(kb + 1) * sa_ld;
         sa_lane = __ldg(sak + (rbase - r8) + lane);
         sb4_next = __ldg(reinterpret_cast<const float4*>(sb + static_cast<int64_t>(kb + 1) * sb_ld_kb + col0) + lane);
@@ -302,6 +342,36 @@ __device__ __forceinline__ void promote_per_column(SharedStorageT<1>& sm, uint32
       }
     }
     if (!alive) break;
+    if (kSplit && U.part >= 0) {
+      // A split tile: hand this part's fp32 partial over through the
+      // workspace; the warp whose part arrives last for its 32 x 128 region
+      // sums all k partials in part order (the same bits whichever part is
+      // last) and stores the region.
+      const int t = ew * 32 + lane;
+      float2* slot = sp.ws + static_cast<int64_t>(U.t_idx * sp.k + U.part) * (64 * 256) + t;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) slot[j * 256] = acc[j];
+      __threadfence();
+      __syncwarp();
+      int arrived = 0;
+      if (lane == 0) arrived = atomicAdd(&sp.cnt[U.t_idx * NUM_EPI_WARPS + ew], 1);
+      arrived = __shfl_sync(0xffffffffu, arrived, 0);
+      if (arrived != sp.k - 1) continue;
+      __threadfence();
+      const float2* first = sp.ws + static_cast<int64_t>(U.t_idx * sp.k) * (64 * 256) + t;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) acc[j] = __ldcg(first + j * 256);
+      for (int p = 1; p < sp.k; ++p) {
+        const float2* part = first + static_cast<int64_t>(p) * (64 * 256);
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const float2 v = __ldcg(part + j * 256);
+          acc[j] = make_float2(acc[j].x + v.x, acc[j].y + v.y);
+        }
+      }
+      if (lane == 0) sp.cnt[U.t_idx * NUM_EPI_WARPS + ew] = 0;  // ready for the next call
+      __syncwarp();
+    }
     if (out_acc != nullptr) {
       // Gradient accumulation: add the tile to the caller's fp32 dW.
 #pragma unroll
@@ -375,13 +445,17 @@ __device__ __forceinline__ void stg_2x16(void* p, const uint32_t (&w)[8]) {
 // kBmn (one-scale-per-block kernel only): 1 = operand B is given MN-major,
 // b[k][n] over [Kc, No] (the dgrad weight read from its row-major codes),
 // loaded as two 128-column boxes and fed to the MMA with "transpose B".
-template <int kBScale, int kQuantOut, int kBmn>
+// kSplit (per-column-scale kernel only): the work-unit loop with the
+// contraction split of the last round (SplitK); without it the loops run over
+// whole tiles, as compiled before the split existed (the unit loop costs a few
+// per cent even when nothing is split).
+template <int kBScale, int kQuantOut, int kBmn, bool kSplit = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     blockwise_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                           const __grid_constant__ CUtensorMap tma_out,
                           const float* __restrict__ sa, int64_t sa_ld, const float* __restrict__ sb, int64_t sb_ld_nb,
                           int64_t sb_ld_kb, uint16_t* __restrict__ out, float* __restrict__ out_acc, QuantOut qo,
-                          int Mo, int No, int Kc, int* status) {
+                          SplitK sp, int Mo, int No, int Kc, int* status) {
   static_assert(kQuantOut == 0 || kBScale == 0, "output quantization is implemented for the fwd/dgrad kernel");
   static_assert(kBmn == 0 || kBScale == 0, "an MN-major B is implemented for the fwd/dgrad kernel");
   extern __shared__ uint8_t smem_raw[];
@@ -392,6 +466,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_m = Mo / BM, num_n = No / BN, num_k = Kc / BK;
   const int num_tiles = num_m * num_n;
+  // Work units: whole tiles, then the contraction parts of the split tail
+  // (the per-column-scale kernel only; sp.k = 1 leaves num_units = num_tiles).
+  static_assert(!kSplit || kBScale == 1, "the contraction split is implemented for the wgrad kernel");
+  const int num_units = kSplit ? sp.full_units + (num_tiles - sp.full_units) * sp.k : num_tiles;
   const AbortFlag ab{&sm.abort_flag};
 
   if (threadIdx.x == 0) {
@@ -434,10 +512,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       uint32_t issued = 0;  // loads issued so far
       bool alive = true;
-      for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < num_units && alive; u += gridDim.x) {
+        const Unit U = kSplit ? unit_of(u, sp, num_k) : Unit{u, 0, num_k, -1, 0};
         int mb, nb;
-        tile_coords<group_m<kBScale>()>(tile, num_m, num_n, mb, nb);
-        for (int kb = 0; kb < num_k; ++kb) {
+        tile_coords<group_m<kBScale>()>(U.tile, num_m, num_n, mb, nb);
+        for (int kb = U.kb0; kb < U.kb1; ++kb) {
           if (!mbar_wait(&sm.empty[stage], phase ^ 1u, ab, status)) {
             alive = false;
             break;
@@ -495,8 +574,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                     : sdesc_kmajor_sw128(smem_u32(sm.b[0]));
       bool alive = true;
       uint32_t g = 0;  // running block index over this CTA's tiles
-      for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
-        for (int kb = 0; kb < num_k; ++kb, ++g) {
+      for (int u = blockIdx.x; u < num_units && alive; u += gridDim.x) {
+        const Unit U = kSplit ? unit_of(u, sp, num_k) : Unit{u, 0, num_k, -1, 0};
+        for (int kb = U.kb0; kb < U.kb1; ++kb, ++g) {
           if ((g & 1u) != static_cast<uint32_t>(me)) continue;
           const int stage = static_cast<int>(g % STAGES);
           const uint32_t phase = (g / STAGES) & 1u;
@@ -532,8 +612,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int half = ew >> 2;                  // column half of the tile
     const int quarter = warp & 3;              // TMEM lane quarter this warp may access
     if constexpr (kBScale == 1) {
-      promote_per_column(sm, tmem, ew, half, quarter, lane, num_tiles, num_m, num_n, num_k, sa, sa_ld, sb, sb_ld_kb,
-                         out, out_acc, No, status, ab);
+      promote_per_column<kSplit>(sm, tmem, ew, half, quarter, lane, num_units, num_m, num_n, num_k, sa, sa_ld, sb, sb_ld_kb,
+                         out, out_acc, No, sp, status, ab);
     } else {
       const int row = quarter * 32 + lane;       // row of the tile this thread owns
       const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
@@ -751,6 +831,38 @@ bool encode_out_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t c
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The split is chosen by a cost model in units of one 128-deep block's time:
+// the tail's rounds of parts, each part costing its blocks plus about kIo
+// block-times of writing its 128 KB fp32 partial, and the last part reading
+// the others'.  k is capped at 16 (the workspace grows with it).
+WgradSplitPlan wgrad_split_plan(int64_t Mo, int64_t No, int64_t Kc, int num_sms) {
+  const int num_tiles = static_cast<int>((Mo / BM) * (No / BN)), num_k = static_cast<int>(Kc / BK);
+  WgradSplitPlan best{num_tiles, 0, 1, 0};
+  if (num_sms <= 0 || num_tiles <= 0) return best;
+  const int rounds = num_tiles / num_sms, tail = num_tiles - rounds * num_sms;
+  if (tail == 0 || num_k < 2) return best;
+  constexpr long kIo = 6;
+  // The split kernel's work-unit loop runs about 5 % slower per block than
+  // the whole-tile one, so a split must save more than that.
+  const long whole = static_cast<long>(rounds + 1) * num_k;
+  long best_cost = whole;
+  for (int k = 2; k <= 16 && k <= num_k; ++k) {
+    const long sub_rounds = (static_cast<long>(tail) * k + num_sms - 1) / num_sms;
+    const long part = (num_k + k - 1) / k;
+    const long cost = (static_cast<long>(rounds) * num_k + sub_rounds * (part + kIo) + kIo * (k - 1)) * 105 / 100;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best.k = k;
+    }
+  }
+  if (best.k == 1) return best;
+  best.full_units = rounds * num_sms;
+  best.tail = tail;
+  const size_t partials = static_cast<size_t>(tail) * best.k * BM * BN * sizeof(float);
+  best.bytes = partials + static_cast<size_t>(tail) * NUM_EPI_WARPS * sizeof(int);
+  return best;
+}
+
 cudaError_t launch_blockwise_gemm(const BlockwiseGemmArgs& g, cudaStream_t st) {
   CUtensorMap ta, tb, to;
   // B K-major: [No, Kc], boxes of BN rows x 128 bytes; MN-major: [Kc, No]
@@ -761,17 +873,34 @@ cudaError_t launch_blockwise_gemm(const BlockwiseGemmArgs& g, cudaStream_t st) {
   if (g.b_scale == BScale::kBlock128x128 && !encode_out_bf16(&to, g.out, g.Mo, g.No)) return cudaErrorInvalidValue;
   if (g.b_scale != BScale::kBlock128x128) to = ta;  // unused by the per-column kernel
   const int num_tiles = static_cast<int>((g.Mo / BM) * (g.No / BN));
-  const int grid = num_tiles < g.num_sms ? num_tiles : g.num_sms;
+  int grid = num_tiles < g.num_sms ? num_tiles : g.num_sms;
+  SplitK sp{num_tiles, 1, nullptr, nullptr};
+  if (g.b_scale == BScale::kPerRow && g.out_acc == nullptr && g.split_ws != nullptr) {
+    const WgradSplitPlan pl = wgrad_split_plan(g.Mo, g.No, g.Kc, g.num_sms);
+    if (pl.k > 1) {
+      if (g.split_ws_bytes < pl.bytes) return cudaErrorInvalidValue;
+      uint8_t* ws = static_cast<uint8_t*>(g.split_ws);
+      sp = SplitK{pl.full_units, pl.k, reinterpret_cast<float2*>(ws),
+                  reinterpret_cast<int*>(ws + (pl.bytes - static_cast<size_t>(pl.tail) * NUM_EPI_WARPS * sizeof(int)))};
+      const cudaError_t e = cudaMemsetAsync(sp.cnt, 0, static_cast<size_t>(pl.tail) * NUM_EPI_WARPS * sizeof(int), st);
+      if (e != cudaSuccess) return e;
+      const int units = pl.full_units + pl.tail * pl.k;
+      grid = units < g.num_sms ? units : g.num_sms;
+    }
+  }
   const QuantOut qo{g.q_out, g.s_out, g.qT_out, g.sT_out};
   const int Mo = static_cast<int>(g.Mo), No = static_cast<int>(g.No), Kc = static_cast<int>(g.Kc);
   auto launch = [&](auto kernel, size_t smem) -> cudaError_t {
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     kernel<<<grid, NUM_THREADS, smem, st>>>(ta, tb, to, g.sa, g.sa_ld, g.sb, g.sb_ld_nb, g.sb_ld_kb, g.out, g.out_acc,
-                                            qo, Mo, No, Kc, g.status);
+                                            qo, sp, Mo, No, Kc, g.status);
     return cudaGetLastError();
   };
-  if (g.b_scale != BScale::kBlock128x128) return launch(blockwise_gemm_kernel<1, 0, 0>, smem_bytes<1>());
+  if (g.b_scale != BScale::kBlock128x128) {
+    if (sp.k > 1) return launch(blockwise_gemm_kernel<1, 0, 0, true>, smem_bytes<1>());
+    return launch(blockwise_gemm_kernel<1, 0, 0>, smem_bytes<1>());
+  }
   if (g.b_mn_major) return launch(blockwise_gemm_kernel<0, 0, 1>, smem_bytes<0>());
   if (g.q_out == nullptr) return launch(blockwise_gemm_kernel<0, 0, 0>, smem_bytes<0>());
   if (g.qT_out == nullptr) return launch(blockwise_gemm_kernel<0, 1, 0>, smem_bytes<0>());

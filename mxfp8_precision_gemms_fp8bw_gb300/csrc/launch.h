@@ -45,11 +45,24 @@ struct BlockwiseGemmArgs {
   float* s_out;
   uint8_t* qT_out;
   float* sT_out;
+  // kPerRow with out_acc null, may be null: workspace for the contraction
+  // split of the last round of tiles (wgrad_split_plan(...).bytes).
+  void* split_ws;
+  size_t split_ws_bytes;
   int64_t Mo, No, Kc;
   int* status;
   int num_sms;
 };
 cudaError_t launch_blockwise_gemm(const BlockwiseGemmArgs& args, cudaStream_t st);
+
+// How the per-column-scale (wgrad) kernel splits its last round of tiles on
+// num_sms SMs: full_units whole tiles, then each of the `tail` remaining tiles
+// in k contraction parts (k = 1: no split); bytes of workspace it needs.
+struct WgradSplitPlan {
+  int full_units, tail, k;
+  size_t bytes;
+};
+WgradSplitPlan wgrad_split_plan(int64_t Mo, int64_t No, int64_t Kc, int num_sms);
 
 struct MxGroupedGemmArgs {
   int kind;                   // 0 fwd, 1 dgrad, 2 wgrad

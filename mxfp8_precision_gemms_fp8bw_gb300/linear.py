@@ -72,7 +72,7 @@ def backward(dy: torch.Tensor, x_col, wq: QuantizedWeight, stream=None, dW_acc: 
         B.fp8bw_gemm_wgrad_acc_f32(dyqT, dysT, xqT, xsT, dW_acc, stream)
         return dx, dW_acc
     dW = torch.empty((N, K), dtype=torch.bfloat16, device=dy.device)
-    B.fp8bw_gemm_wgrad(dyqT, dysT, xqT, xsT, dW, stream)
+    B.fp8bw_gemm_wgrad_ws(dyqT, dysT, xqT, xsT, dW, B.alloc_wgrad_workspace(M, N, K, dy.device), stream)
     return dx, dW
 
 
@@ -187,6 +187,7 @@ class BlockwiseLinearWorkspace:
         self.dyqT, self.dysT = e((N, M), u8), e((M // 128, N), f32)
         self.xqT, self.xsT = e((K, M), u8), e((M // 128, K), f32)
         self.dW = e((N, K), bf)
+        self.wgrad_ws = B.alloc_wgrad_workspace(M, N, K, device)  # tail split of wgrad (None if not needed)
 
     def kernels(self, x, w, dy, stream=None):
         return [
@@ -198,7 +199,8 @@ class BlockwiseLinearWorkspace:
              lambda: B.fp8bw_quant_1x128_rowcol(dy, self.dyq, self.dys, self.dyqT, self.dysT, stream)),
             ("gemm_dgrad",
              lambda: B.fp8bw_gemm_dgrad(self.dyq, self.dys, self.wq, self.wqT, self.ws, self.dx, stream)),
-            ("gemm_wgrad", lambda: B.fp8bw_gemm_wgrad(self.dyqT, self.dysT, self.xqT, self.xsT, self.dW, stream)),
+            ("gemm_wgrad",
+             lambda: B.fp8bw_gemm_wgrad_ws(self.dyqT, self.dysT, self.xqT, self.xsT, self.dW, self.wgrad_ws, stream)),
         ]
 
     def step(self, x, w, dy, stream=None):
@@ -382,6 +384,9 @@ class ToyFFNStep:
             e((M, hidden), bf)
         self.dx1, self.dx2, self.dx = e((M, dim), bf), e((M, dim), bf), e((M, dim), bf)
         self.d_w1, self.d_w2, self.d_wo = e((hidden, dim), bf), e((hidden, dim), bf), e((dim, hidden), bf)
+        # one workspace for the three wgrads (they run one after another on one stream)
+        sizes = [B.fp8bw_gemm_wgrad_workspace_bytes(M, dim, hidden), B.fp8bw_gemm_wgrad_workspace_bytes(M, hidden, dim)]
+        self.wgrad_ws = e((max(sizes),), u8) if max(sizes) else None
 
     @staticmethod
     def _rowcol(src, a, stream):
@@ -414,14 +419,16 @@ class ToyFFNStep:
             ("gemm_dgrad(out_proj)",
              lambda: B.fp8bw_gemm_dgrad(dya["q"], dya["s"], qo.q, qo.qT, qo.s, self.da, stream)),
             ("gemm_wgrad(out_proj)",
-             lambda: B.fp8bw_gemm_wgrad(dya["qT"], dya["sT"], aa["qT"], aa["sT"], self.d_wo, stream)),
+             lambda: B.fp8bw_gemm_wgrad_ws(dya["qT"], dya["sT"], aa["qT"], aa["sT"], self.d_wo, self.wgrad_ws, stream)),
             ("act grad (torch)", self._act_grad),
             ("quant_1x128_rowcol(dh1)", self._rowcol(self.dh1, d1, stream)),
             ("quant_1x128_rowcol(dh2)", self._rowcol(self.dh2, d2, stream)),
             ("gemm_dgrad(w1)", lambda: B.fp8bw_gemm_dgrad(d1["q"], d1["s"], q1.q, q1.qT, q1.s, self.dx1, stream)),
-            ("gemm_wgrad(w1)", lambda: B.fp8bw_gemm_wgrad(d1["qT"], d1["sT"], xa["qT"], xa["sT"], self.d_w1, stream)),
+            ("gemm_wgrad(w1)",
+             lambda: B.fp8bw_gemm_wgrad_ws(d1["qT"], d1["sT"], xa["qT"], xa["sT"], self.d_w1, self.wgrad_ws, stream)),
             ("gemm_dgrad(w2)", lambda: B.fp8bw_gemm_dgrad(d2["q"], d2["s"], q2.q, q2.qT, q2.s, self.dx2, stream)),
-            ("gemm_wgrad(w2)", lambda: B.fp8bw_gemm_wgrad(d2["qT"], d2["sT"], xa["qT"], xa["sT"], self.d_w2, stream)),
+            ("gemm_wgrad(w2)",
+             lambda: B.fp8bw_gemm_wgrad_ws(d2["qT"], d2["sT"], xa["qT"], xa["sT"], self.d_w2, self.wgrad_ws, stream)),
             ("dx sum (torch)", lambda: torch.add(self.dx1, self.dx2, out=self.dx)),
         ]
 

@@ -29,6 +29,7 @@ def test_header_declares_the_abi():
     assert names == sorted([
         "fp8bw_quant_1x128_row", "fp8bw_quant_1x128_col", "fp8bw_quant_128x128", "fp8bw_quant_1x128_rowcol",
         "fp8bw_gemm_fwd", "fp8bw_gemm_fwd_quant", "fp8bw_gemm_dgrad", "fp8bw_gemm_wgrad", "fp8bw_gemm_wgrad_acc_f32",
+        "fp8bw_gemm_wgrad_ws", "fp8bw_gemm_wgrad_workspace_bytes",
         "mxfp8_quant_1x32_row", "mxfp8_quant_1x32_col", "mxfp8_quant_3d_col", "mxfp8_grouped_gemm",
         "mxfp8_grouped_gemm_workspace_bytes", "mxfp8_grouped_gemm_noalloc",
         "fp8bw_sync_status", "fp8bw_last_error", "fp8bw_selftest_bounded_wait",

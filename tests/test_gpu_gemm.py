@@ -177,3 +177,74 @@ def test_dgrad_from_q_equals_dgrad_from_qT(M, N, K, seed):
     woq, _, wos = oracle.quant_128x128(wf)
     dd, wdq = oracle.dequant_1x128_row(oq, os_), oracle.dequant_128x128(woq, wos)
     assert gemm_max_err(f32(dx_q)[rows], dd @ wdq, dd, wdq.T) <= TOL
+
+
+def _wgrad_case(M, N, K, seed):
+    t = inputs.linear_inputs(M, K, N, seed=seed)
+    dyd, xd = t.dy.cuda(), t.x.cuda()
+    dyqT, dysT = B.alloc_quant_1x128_col(dyd)
+    B.fp8bw_quant_1x128_col(dyd, dyqT, dysT)
+    xqT, xsT = B.alloc_quant_1x128_col(xd)
+    B.fp8bw_quant_1x128_col(xd, xqT, xsT)
+    return t, dyqT, dysT, xqT, xsT
+
+
+@pytest.mark.parametrize("M,N,K,seed", [(8192, 1536, 4096, 0), (5632, 1536, 4096, 1)])
+def test_wgrad_split_tail(M, N, K, seed):
+    # 192 output tiles: on 152 SMs the last 40 run as contraction parts (64 or
+    # 44 blocks over 3 parts: lengths 21/21/22 and 14/15/15).  The parts' fp32
+    # partials are added in part order, so two calls give the same bits; the
+    # result is within the bar of the oracle.
+    assert torch.cuda.get_device_properties(0).multi_processor_count == 152
+    t, dyqT, dysT, xqT, xsT = _wgrad_case(M, N, K, 500 + seed)
+    ws = B.alloc_wgrad_workspace(M, N, K, dyqT.device)
+    assert ws is not None and ws.numel() > 0
+    outs = []
+    for _ in range(2):
+        dW = torch.full((N, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+        B.fp8bw_gemm_wgrad_ws(dyqT, dysT, xqT, xsT, dW, ws)
+        B.fp8bw_sync_status()
+        outs.append(dW)
+    assert torch.equal(outs[0], outs[1])
+    dq, ds = oracle.quant_1x128_col(f32(t.dy))
+    xq, xs = oracle.quant_1x128_col(f32(t.x))
+    dd, xdq = oracle.dequant_1x128_row(dq, ds), oracle.dequant_1x128_row(xq, xs)
+    assert gemm_max_err(f32(outs[0]), dd @ xdq.T, dd, xdq) <= TOL
+    # without a workspace the same call is the plain wgrad
+    dW2 = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    B.fp8bw_gemm_wgrad_ws(dyqT, dysT, xqT, xsT, dW2, None)
+    dW3 = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    B.fp8bw_gemm_wgrad(dyqT, dysT, xqT, xsT, dW3)
+    B.fp8bw_sync_status()
+    assert torch.equal(dW2, dW3)
+
+
+def test_wgrad_split_large_token_against_whole_tiles():
+    # The large-token wgrad (M = 128000 contracted, 240 output tiles: the last
+    # 88 split in five contraction parts) against the whole-tile kernel on
+    # every element.  (Its parity against the oracle is checked on sampled
+    # outputs by the large-token linear test, which runs the same call.)
+    M, K, N = 128000, 5120, 1536
+    assert B.fp8bw_gemm_wgrad_workspace_bytes(M, N, K) > 0
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    dy = (torch.randn((M, N), generator=g, device="cuda") * 1e-3).bfloat16()
+    x = torch.randn((M, K), generator=g, device="cuda").bfloat16()
+    dyqT, dysT = B.alloc_quant_1x128_col(dy)
+    B.fp8bw_quant_1x128_col(dy, dyqT, dysT)
+    xqT, xsT = B.alloc_quant_1x128_col(x)
+    B.fp8bw_quant_1x128_col(x, xqT, xsT)
+    ws = B.alloc_wgrad_workspace(M, N, K, dy.device)
+    dW = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    B.fp8bw_gemm_wgrad_ws(dyqT, dysT, xqT, xsT, dW, ws)
+    # the tail's fp32 partial sums are added in another order (a difference of
+    # a few fp32 ulps of the sum of |partials|, far below 1e-5 of the matrix's
+    # largest value), which can move the bf16 rounding by one ulp (2^-7 of the
+    # value); nothing else differs
+    dW_plain = torch.empty_like(dW)
+    B.fp8bw_gemm_wgrad(dyqT, dysT, xqT, xsT, dW_plain)
+    B.fp8bw_sync_status()
+    p = dW_plain.float()
+    d = (dW.float() - p).abs()
+    assert bool((d <= p.abs() * 2.0 ** -7 + 1e-5 * float(p.abs().max())).all())
+    assert float((d > 0).float().mean()) < 0.01
