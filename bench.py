@@ -518,9 +518,12 @@ def run_moe(dev, steps, warmup, fp8_peak, hbm_peak, world, dense: bool = False):
     }
 
 
-def section_from_times(workload, per, algo, flops, ms_step, steps, fp8_peak, hbm_peak, fwd_names, world, extra=None):
+def section_from_times(workload, per, algo, flops, ms_step, steps, fp8_peak, hbm_peak, fwd_names, world, extra=None,
+                       traffic_key=None):
     """One bench section: whole-step TFLOP/s, per-call times and roofline
-    fractions, the dominant GEMM, and the per-linear microseconds."""
+    fractions, the dominant GEMM, and the per-linear microseconds.  The
+    dominant GEMM's DRAM traffic comes from the ncu summary under
+    `traffic_key` (``<section>/<kernel>``) when one was taken on this shape."""
     gemm_names = [n for n in per if algo[n][0] == "flops"]
     dom = max(gemm_names, key=lambda n: per[n])
     dom_ach = algo[dom][1] / (per[dom] * 1e-3) / 1e12
@@ -531,7 +534,8 @@ def section_from_times(workload, per, algo, flops, ms_step, steps, fp8_peak, hbm
         "gpu_launches": sum(1 for n in per if algo[n][0] is not None) * steps,
         "gemm_tflops": round(flops / (sum(per[n] for n in gemm_names) * 1e-3) / 1e12, 1),
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(dom_ach, 1), "peak": round(fp8_peak, 1),
-                     "unit": "TFLOP/s", "frac": round(dom_ach / fp8_peak, 4), "traffic": None},
+                     "unit": "TFLOP/s", "frac": round(dom_ach / fp8_peak, 4),
+                     "traffic": load_traffic(f"{traffic_key}/{dom}") if traffic_key else None},
         "kernels": kernel_table(per, algo, fp8_peak, hbm_peak),
         "linear_us": linear_us(per, fwd_names),
     }
@@ -568,7 +572,8 @@ def run_large_token(dev, which, steps, warmup, fp8_peak, hbm_peak, world):
     workload = (f"large-token dense Float8BlockwiseLinear fwd+bwd, M={Mt} K={Kt} N={Nt} (wgrad contracts over "
                 f"{Mt} tokens), x~N(0,1) W~N(0,0.02) dy~N(0,1e-3) drawn on the device, seed 3")
     sec = section_from_times(workload, per, ws.algorithmic(), 6 * Mt * Nt * Kt, ms_step, steps, fp8_peak, hbm_peak,
-                             ["quant_1x128_rowcol(x)", "quant_128x128(W)", "gemm_fwd"], world)
+                             ["quant_1x128_rowcol(x)", "quant_128x128(W)", "gemm_fwd"], world,
+                             traffic_key=f"large{which}")
     del x, w, dy, ws, kern
     torch.cuda.empty_cache()
     return sec
@@ -764,6 +769,43 @@ def load_traffic(kernel: str):
         return None
 
 
+def run_section(args, world, local):
+    """One workload's step alone (see --section): a single JSON line."""
+    import torch
+
+    from mxfp8_precision_gemms_fp8bw_gb300 import binding as B
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.lib(build_if_missing=True)
+    peaks = load_peaks()
+    fp8_peak, hbm = peaks["bf16"] * FP8_OVER_BF16, peaks["hbm_gbs"]
+    steps, warmup = args.steps, args.warmup
+    if args.section == "dense":
+        from mxfp8_precision_gemms_fp8bw_gb300.linear import BlockwiseLinearWorkspace
+        t = dense_inputs()
+        x, w, dy = t.x.to(dev), t.w.to(dev), t.dy.to(dev)
+        ws = BlockwiseLinearWorkspace(M, N, K, device=dev)
+        kern = ws.kernels(x, w, dy)
+        for _ in range(warmup):
+            ws.step(x, w, dy)
+        B.fp8bw_sync_status()
+        ms, per = time_kernels(kern, steps, torch.cuda.current_stream(dev))
+        B.fp8bw_sync_status()
+        sec = section_from_times(WORKLOAD, per, ws.algorithmic(), 6 * M * N * K, ms, steps, fp8_peak, hbm,
+                                 ["quant_1x128_rowcol(x)", "quant_128x128(W)", "gemm_fwd"], world)
+    elif args.section in ("large0", "large1"):
+        sec = run_large_token(dev, int(args.section[-1]), steps, warmup, fp8_peak, hbm, world)
+    elif args.section == "ffn":
+        sec = run_ffn(dev, steps, warmup, fp8_peak, hbm, world)
+    elif args.section == "chain":
+        sec = run_chain_epilogue_quant(dev, steps, warmup, fp8_peak, hbm, world)
+    else:
+        sec = run_moe(dev, steps, warmup, fp8_peak, hbm, world, dense=args.section == "mxdense")
+    print(json.dumps({"section": args.section, **sec}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -772,18 +814,24 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-moe", action="store_true", help="skip the MXFP8 sections (MoE and dense)")
+    ap.add_argument("--section", choices=["dense", "large0", "large1", "ffn", "chain", "moe", "mxdense"],
+                    help="run only this workload's step (--warmup untimed, --steps timed) and print its section as "
+                         "one JSON line: for profiling one kernel on one workload")
     ap.add_argument("--tables", action="store_true",
                     help="instead of the bench line, time the blockwise linear over the dense and large-token "
                          "shapes and the MXFP8 grouped linear over the shapes of the grouped-mm microbenchmark "
                          "table (one JSON line per shape)")
     args = ap.parse_args()
-    args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
+    if not args.section:
+        args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     if args.impl == "reference":
         # Rank 0 alone times the CPU oracle; the other ranks exit without work
         # (no process group: nothing is exchanged).
         world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
         return run_reference(args, world, rank)
     world, rank, local = dist_setup(args.gpus)
+    if args.section:
+        return run_section(args, world, local)
     if args.tables:
         import torch
         torch.cuda.set_device(local)
