@@ -317,13 +317,12 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
       : "r"(taddr));
 }
 
-// 16 lanes x 32 consecutive 32-bit columns (four 16x256b chunks).  Thread
-// t of the warp receives, for chunk c (columns col + 8c ...), the four values
-// (lane t/4, column 2(t%4)), (t/4, 2(t%4)+1), (t/4 + 8, 2(t%4)), (t/4 + 8,
-// 2(t%4)+1) in r[4c .. 4c+3] -- the layout of an m16n8 accumulator fragment.
-__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+// 16 lanes x 32 consecutive 32-bit columns as eight 16x128b chunks.  Thread
+// t receives, for chunk c (columns col + 4c ...), (lane t/4, column 4c + t%4)
+// in r[2c] and (lane t/4 + 8, column 4c + t%4) in r[2c + 1].
+__device__ __forceinline__ void tmem_ld_16x128b_x8(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "tcgen05.ld.sync.aligned.16x128b.x8.b32 "
       "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])

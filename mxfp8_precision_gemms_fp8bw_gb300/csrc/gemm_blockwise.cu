@@ -33,7 +33,7 @@
 //               through its shared staging area by two TMA stores that
 //               complete while the warp promotes the next tile; with one B
 //               scale per column (wgrad) a thread owns 4 rows x 32 columns
-//               (16x256b loads), which divides the broadcast reads of the
+//               (16x128b loads), which divides the broadcast reads of the
 //               column scales by four.
 // The MMA of block kb+1 runs while block kb is being promoted.
 //
@@ -90,9 +90,10 @@ struct SharedStorageT {
   uint8_t b[S][B_BYTES];
   uint8_t epi[NUM_EPI_WARPS][EPI];
   // Per-column B scales of the current and next block (per-column-scale
-  // kernel only), private to each promotion warp: [warp][buffer][SB_STRIDE * q + 2 * chunk + e] holds column
-  // 8 * chunk + 2 * q + e (q = lane % 4), so a thread's 32 scales are
-  // contiguous and its 16-byte loads of two chunks hit distinct banks.
+  // kernel only), private to each promotion warp: [warp][buffer][SB_STRIDE * q + i]
+  // holds column 4 * i + q of the warp's 128 (q = lane % 4), so a thread's 32
+  // scales are contiguous and the four lane classes' 16-byte loads hit
+  // distinct banks.
   float sb_vec[NUM_EPI_WARPS][2][4 * SB_STRIDE];
   uint64_t full[S];
   uint64_t empty[S];
@@ -145,8 +146,8 @@ __device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
   return v;
 }
-__device__ __forceinline__ void sts_f32x2(uint32_t addr, float a, float b) {
-  asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+__device__ __forceinline__ void sts_f32(uint32_t addr, float a) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(a) : "memory");
 }
 
 // Byte offset of 16-byte chunk k (0..7) of row r in a box of 128-byte rows
@@ -178,10 +179,10 @@ __device__ __forceinline__ void store_box(uint32_t stage, uint16_t* __restrict__
   }
 }
 
-__device__ __forceinline__ void sts_b32(uint32_t addr, uint32_t a) {
-  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
+__device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t a) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(a) : "memory");
 }
-
+__device__ __forceinline__ uint16_t bf16_bits(float x) { return static_cast<uint16_t>(pack_bf16x2(x, 0.0f) & 0xFFFFu); }
 // Contraction split of the last round of wgrad tiles.  The first full_units
 // work units are whole tiles; the remaining tiles (when the tile count is not
 // a multiple of the grid) are each cut into k contraction ranges, so the last
@@ -223,12 +224,11 @@ __device__ __forceinline__ Unit unit_of(int u, const SplitK& sp, int num_k) {
 // Promotion with a per-column B scale (wgrad: both operands in 1x128 blocks
 // along the contraction), out[i, j] = sum_kb sa[kb][i] * sb[kb][j] * P_kb[i, j].
 // Every column of a block has its own scale, which every row needs.  Reading
-// the partial with the 16x256b TMEM shape gives each thread 4 rows x 32
-// columns (two adjacent columns of every 8), so it needs 32 of the 128 column
-// scales.  They are staged per warp in a layout where those 32 are
-// contiguous: one conflict-free 16-byte shared load covers two chunks for
-// both lane halves (8 loads per thread per block).  Shared-memory loads
-// compete with the tensor core's operand reads, so they are kept this few.
+// the partial with the 16x128b TMEM shape gives each thread 4 rows x 32
+// columns (one column of every 4), so it needs 32 of the 128 column scales,
+// staged per warp so that a thread's 32 are contiguous (8 conflict-free
+// 16-byte shared loads per thread per block).  The two rows of a load that
+// share a column are folded in as one packed pair.
 template <bool kSplit>
 __device__ __forceinline__ void promote_per_column(SharedStorageT<1>& sm, uint32_t tmem, int ew, int half, int quarter,
                                                    int lane, int num_units, int num_m, int num_n, int num_k,
@@ -246,7 +246,7 @@ __device__ __forceinline__ void promote_per_column(SharedStorageT<1>& sm, uint32
     tile_coords<group_m<1>()>(U.tile, num_m, num_n, mb, nb);
     const int64_t rbase = static_cast<int64_t>(mb) * BM + quarter * 32 + r8;  // rows rbase + 16h + 8e
     const int64_t col0 = static_cast<int64_t>(nb) * BN + half * 128;
-    float2 acc[64];  // column pair 2*q4 of chunk k, row 16h + 8e: acc[(h * 16 + k) * 2 + e]
+    float2 acc[64];  // column 32cq + 4j + q4, rows 16h + r8 (x) and 16h + r8 + 8 (y): acc[(h * 4 + cq) * 8 + j]
 #pragma unroll
     for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
 
@@ -261,14 +261,15 @@ __device__ __forceinline__ void promote_per_column(SharedStorageT<1>& sm, uint32
       float sa_cur[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) sa_cur[i] = __shfl_sync(0xffffffffu, sa_lane, r8 + 16 * (i >> 1) + 8 * (i & 1));
-      // The buffer written now was last read two blocks ago; every lane
-      // finished those reads before the previous block's __syncwarp.
       {
-        // Lane L holds columns 4L .. 4L + 3: chunk L / 2, quarters 2 (L % 2)
-        // and 2 (L % 2) + 1.
-        const uint32_t dst = smem_u32(sm.sb_vec[ew][kb & 1] + (2 * (lane & 1)) * SB_STRIDE + 2 * (lane >> 1));
-        sts_f32x2(dst, sb4_next.x, sb4_next.y);
-        sts_f32x2(dst + SB_STRIDE * 4, sb4_next.z, sb4_next.w);
+        // Lane L holds columns 4L .. 4L + 3 = 32cq + 4j + e with cq * 8 + j = L.
+        // The buffer written now was last read two blocks ago; every lane
+        // finished those reads before the previous block's __syncwarp.
+        const uint32_t dst = smem_u32(sm.sb_vec[ew][kb & 1] + lane);
+        sts_f32(dst, sb4_next.x);
+        sts_f32(dst + 4 * SB_STRIDE, sb4_next.y);
+        sts_f32(dst + 8 * SB_STRIDE, sb4_next.z);
+        sts_f32(dst + 12 * SB_STRIDE, sb4_next.w);
       }
       __syncwarp();
       if (kb + 1 < U.kb1) {
@@ -283,56 +284,35 @@ __device__ __forceinline__ void promote_per_column(SharedStorageT<1>& sm, uint32
       tc_fence_after();
       const uint32_t t_col = tmem + static_cast<uint32_t>(buf * BN + half * 128);
       const uint32_t sbv = smem_u32(sm.sb_vec[ew][kb & 1] + q4 * SB_STRIDE);
-      // Load/wait rounds over the warp's 128 columns: each round takes kCqr
-      // column quarters (chunks 4cq .. 4cq + 3) for both 16-lane halves h of
-      // the warp's 32 TMEM lanes, then one wait.  The scales of a column
-      // quarter serve both halves.
-      // One column quarter per round: wider rounds (more loads before a wait)
-      // measured no faster, the partial's TMEM reads being what sets the pace.
-      constexpr int kCqr = 1;
+      const float2 fa[2] = {make_float2(sa_cur[0], sa_cur[1]), make_float2(sa_cur[2], sa_cur[3])};
+      // One load/wait round per column quarter cq (columns 32cq .. 32cq + 31)
+      // for both 16-lane halves h of the warp's 32 TMEM lanes; the quarter's
+      // scales serve both halves.  Wider rounds, or the next round's loads
+      // issued before this round's products, measured no faster: the
+      // partial's TMEM reads, which share TMEM with the MMAs, set the pace.
 #pragma unroll
-      for (int rr = 0; rr < 4 / kCqr; ++rr) {
-        float2 sc[kCqr][4];
+      for (int cq = 0; cq < 4; ++cq) {
+        const float4 s0 = lds_f32x4(sbv + 32 * cq);
+        const float4 s1 = lds_f32x4(sbv + 32 * cq + 16);
+        const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        uint32_t r[2][16];
 #pragma unroll
-        for (int c2 = 0; c2 < kCqr; ++c2) {
-          const int cq = rr * kCqr + c2;
-          const float4 s01 = lds_f32x4(sbv + 32 * cq);       // chunks 4cq, 4cq + 1
-          const float4 s23 = lds_f32x4(sbv + 32 * cq + 16);  // chunks 4cq + 2, 4cq + 3
-          sc[c2][0] = make_float2(s01.x, s01.y);
-          sc[c2][1] = make_float2(s01.z, s01.w);
-          sc[c2][2] = make_float2(s23.x, s23.y);
-          sc[c2][3] = make_float2(s23.z, s23.w);
-        }
-        uint32_t r[kCqr][2][16];
-#pragma unroll
-        for (int c2 = 0; c2 < kCqr; ++c2)
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            tmem_ld_16x256b_x4(t_col + (static_cast<uint32_t>(quarter * 32 + 16 * h) << 16) + (rr * kCqr + c2) * 32,
-                               r[c2][h]);
+        for (int h = 0; h < 2; ++h)
+          tmem_ld_16x128b_x8(t_col + (static_cast<uint32_t>(quarter * 32 + 16 * h) << 16) + cq * 32, r[h]);
         tmem_ld_wait();
-        if (rr == 4 / kCqr - 1) {
+        if (cq == 3) {
           // The whole partial is in registers: the buffer goes back to the MMA warp.
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
         }
 #pragma unroll
-        for (int c2 = 0; c2 < kCqr; ++c2) {
+        for (int h = 0; h < 2; ++h) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float2 fa0 = make_float2(sa_cur[h * 2], sa_cur[h * 2]);
-            const float2 fa1 = make_float2(sa_cur[h * 2 + 1], sa_cur[h * 2 + 1]);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int k = (rr * kCqr + c2) * 4 + c;
-              const float2 p0 = make_float2(__uint_as_float(r[c2][h][4 * c]), __uint_as_float(r[c2][h][4 * c + 1]));
-              const float2 p1 = make_float2(__uint_as_float(r[c2][h][4 * c + 2]), __uint_as_float(r[c2][h][4 * c + 3]));
-              float2& a0 = acc[(h * 16 + k) * 2];
-              float2& a1 = acc[(h * 16 + k) * 2 + 1];
-              a0 = __ffma2_rn(__fmul2_rn(p0, sc[c2][c]), fa0, a0);
-              a1 = __ffma2_rn(__fmul2_rn(p1, sc[c2][c]), fa1, a1);
-            }
+          for (int j = 0; j < 8; ++j) {
+            const float2 p = make_float2(__uint_as_float(r[h][2 * j]), __uint_as_float(r[h][2 * j + 1]));
+            float2& a = acc[(h * 4 + cq) * 8 + j];
+            a = __ffma2_rn(__fmul2_rn(p, make_float2(sc[j], sc[j])), fa[h], a);
           }
         }
       }
@@ -376,14 +356,15 @@ __device__ __forceinline__ void promote_per_column(SharedStorageT<1>& sm, uint32
       // Gradient accumulation: add the tile to the caller's fp32 dW.
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
+        float* row0 = out_acc + (rbase + 16 * h) * No + col0 + q4;
+        float* row1 = row0 + 8 * static_cast<int64_t>(No);
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float2* orow = reinterpret_cast<float2*>(out_acc + (rbase + 16 * h + 8 * e) * No + col0 + 2 * q4);
+        for (int cq = 0; cq < 4; ++cq) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float2 v = acc[(h * 16 + k) * 2 + e];
-            const float2 o = orow[4 * k];
-            orow[4 * k] = make_float2(o.x + v.x, o.y + v.y);
+          for (int j = 0; j < 8; ++j) {
+            const float2 v = acc[(h * 4 + cq) * 8 + j];
+            row0[32 * cq + 4 * j] += v.x;
+            row1[32 * cq + 4 * j] += v.y;
           }
         }
       }
@@ -397,12 +378,14 @@ __device__ __forceinline__ void promote_per_column(SharedStorageT<1>& sm, uint32
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int r = 8 * e + r8;  // row within the box
+          for (int c2 = 0; c2 < 2; ++c2) {
 #pragma unroll
-            for (int k8 = 0; k8 < 8; ++k8) {
-              const float2 v = acc[(h * 16 + cc * 8 + k8) * 2 + e];
-              sts_b32(stage + sw128_offset(r, k8) + 4 * q4, pack_bf16x2(v.x, v.y));
+            for (int j = 0; j < 8; ++j) {
+              const float2 v = acc[(h * 4 + 2 * cc + c2) * 8 + j];
+              const int k8 = 4 * c2 + (j >> 1);
+              const uint32_t off = 2 * (4 * (j & 1) + q4);
+              sts_u16(stage + sw128_offset(r8, k8) + off, bf16_bits(v.x));
+              sts_u16(stage + sw128_offset(r8 + 8, k8) + off, bf16_bits(v.y));
             }
           }
           __syncwarp();
