@@ -30,9 +30,16 @@
 //              B: [M/128 + G windows][K/128][512 B]
 // (windows: the 128-token steps of each group, numbered group after group).
 //
-// GEMM CTA (persistent, 384 threads):
-//   warp 0      TMA producer: per stage A 128x128 and B 256x128 e4m3 tiles
-//               (tensor maps) plus their 512 B + 1 KB scale chunks (bulk copies)
+// GEMM CTA (persistent, 384 threads), run in clusters of two CTAs whose
+// tiles share B (consecutive 128-token tiles of one group for FWD/DGRAD,
+// consecutive dW row tiles of one group for WGRAD; a WGRAD with an odd
+// N / 128 runs unpaired):
+//   warp 0      TMA producer: per stage the CTA's A 128x128 tile, one
+//               128-row half of the shared B 256x128 tile, which the TMA
+//               multicast writes into both CTAs (each SM fetches 32 KB of
+//               operands per stage instead of 48 KB), and the 512 B + 1 KB
+//               scale chunks (bulk copies); a stage is refilled once the
+//               MMAs of both CTAs have read it
 //   warp 1      TMEM owner and MMA issuer: up to 4 block-scaled MMAs per
 //               stage (K = 32 each; the instruction descriptor selects scale
 //               byte j)
@@ -82,6 +89,7 @@ struct Problem {
 struct GroupTable {
   int32_t start[MAX_GROUPS + 1];  // token start of each group (sanitized), start[G] = end
   int32_t tile0[MAX_GROUPS + 1];  // first 128-token tile / window of each group; tile0[G] = total
+  int32_t pair0[MAX_GROUPS + 1];  // FWD/DGRAD, CTA pairs: first pair of 128-token tiles of each group
 };
 
 // Clamps every group range into [0, M] and rounds each end down to a multiple
@@ -89,7 +97,7 @@ struct GroupTable {
 // group_end holds).  Returns true when group_end broke the rules (a size that
 // is not a multiple of 32, a decreasing end, or a last end other than M).
 __device__ bool build_group_table(const int32_t* group_end, int G, int M, GroupTable& t) {
-  int prev = 0, tile0 = 0;
+  int prev = 0, tile0 = 0, pair0 = 0;
   bool bad = false;
   for (int g = 0; g < G; ++g) {
     int e = group_end[g];
@@ -97,26 +105,31 @@ __device__ bool build_group_table(const int32_t* group_end, int G, int M, GroupT
     e = max(min(max(e, prev), M) & ~31, prev);
     t.start[g] = prev;
     t.tile0[g] = tile0;
-    tile0 += (e - prev + BM - 1) / BM;
+    t.pair0[g] = pair0;
+    const int tiles = (e - prev + BM - 1) / BM;
+    tile0 += tiles;
+    pair0 += (tiles + 1) / 2;
     prev = e;
   }
   if (prev != M) bad = true;
   t.start[G] = prev;
   t.tile0[G] = tile0;
+  t.pair0[G] = pair0;
   return bad;
 }
 
 // The group owning 128-token tile (or window) i: the last g with tile0[g] <= i
 // (empty groups own no tile and are skipped).
-__device__ __forceinline__ int group_of(const GroupTable& t, int G, int i) {
-  int lo = 0, hi = G;  // invariant: tile0[lo] <= i < tile0[hi]
+__device__ __forceinline__ int group_of_in(const int32_t* first, int G, int i) {
+  int lo = 0, hi = G;  // invariant: first[lo] <= i < first[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (t.tile0[mid] <= i) lo = mid;
+    if (first[mid] <= i) lo = mid;
     else hi = mid;
   }
   return lo;
 }
+__device__ __forceinline__ int group_of(const GroupTable& t, int G, int i) { return group_of_in(t.tile0, G, i); }
 
 struct SharedStorage {
   uint8_t a[STAGES][A_BYTES];
@@ -198,6 +211,82 @@ __device__ __forceinline__ Tile decode(const GroupTable& gt, const Problem& p, i
   return T;
 }
 
+// The tile of CTA `rank` (0 or 1) of a cluster for pair-tile `pt`: the two
+// CTAs take two 128-row tiles that share one 256-row B tile -- consecutive
+// token tiles of one group (FWD/DGRAD; a group with an odd tile count gets a
+// second tile whose rows all lie past the group's end, computed and never
+// stored) or consecutive dW row tiles of one group (WGRAD).
+__device__ __forceinline__ Tile decode_pair(const GroupTable& gt, const Problem& p, int pt, int rank) {
+  Tile T;
+  if (p.kind != 2) {
+    int pm, nt;
+    raster(pt, gt.pair0[p.G], p.num_nt, pm, nt);
+    const int g = group_of_in(gt.pair0, p.G, pm);
+    const int local = 2 * (pm - gt.pair0[g]) + rank;
+    const int tiles = gt.tile0[g + 1] - gt.tile0[g];
+    const int m0 = gt.start[g] + local * BM;
+    T.g = g;
+    T.a_row0 = m0;
+    T.b_row0 = g * p.n_out + nt * BN;
+    T.k_begin = 0;
+    T.k_end = p.kc;
+    T.out_row0 = m0;
+    T.row_limit = gt.start[g + 1];
+    T.out_col0 = nt * BN;
+    // A tile past the group's end reads any valid scale chunk of the group.
+    T.sfa_chunk0 = gt.tile0[g] + min(local, tiles - 1);
+    T.sfa_step = p.mt_max;
+    T.sfb_chunk0 = T.b_row0 / BM;
+    T.sfb_step = p.rb_b;
+  } else {
+    const int rb_a = p.N / BM, rb_b = p.K / BM;
+    const int per_group = (rb_a / 2) * p.num_nt;
+    const int g = pt / per_group;
+    int pm, nt;
+    raster(pt - g * per_group, rb_a / 2, p.num_nt, pm, nt);
+    const int mt = 2 * pm + rank;
+    T.g = g;
+    T.a_row0 = mt * BM;
+    T.b_row0 = nt * BN;
+    T.k_begin = gt.start[g];
+    T.k_end = gt.start[g + 1];
+    T.out_row0 = mt * BM;
+    T.row_limit = p.N;
+    T.out_col0 = nt * BN;
+    T.sfa_chunk0 = static_cast<int64_t>(gt.tile0[g]) * rb_a + mt;
+    T.sfa_step = rb_a;
+    T.sfb_chunk0 = static_cast<int64_t>(gt.tile0[g]) * rb_b + T.b_row0 / BM;
+    T.sfb_step = rb_b;
+  }
+  return T;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 2D tiled load delivered to the same shared-memory offset (data and
+// mbarrier) of every CTA of the cluster in `mask`.
+__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t c0,
+                                                      int32_t c1, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
+      : "memory");
+}
+// tcgen05.commit arriving on the mbarrier at `bar`'s offset in every CTA of `mask`.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "h"(mask)
+               : "memory");
+}
+
 __device__ __forceinline__ int num_kb(const Tile& T) { return (T.k_end - T.k_begin + BK - 1) / BK; }
 
 // 1D bulk copy global -> shared completing `bytes` on `bar` (16-byte aligned).
@@ -277,6 +366,11 @@ __global__ void __launch_bounds__(256) mx_pack_scales_kernel(const uint8_t* __re
 
 // ---------------------------------------------------------------- GEMM
 
+// kPair: the kernel runs in clusters of two CTAs that share each stage's B
+// tile; each CTA loads half of it (128 rows) and the TMA multicast delivers
+// both halves to both CTAs, so each SM fetches 32 KB instead of 48 KB per
+// stage.  Each CTA still issues its own M128 N256 MMAs on its own A tile.
+template <bool kPair>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     mx_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                            const uint32_t* __restrict__ ws_a, const uint32_t* __restrict__ ws_b,
@@ -292,7 +386,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (build_group_table(group_end, p.G, p.M, sm.groups) && blockIdx.x == 0) atomicExch(status, kStatusShape);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      // A stage is free once the MMAs of every CTA that received its B half have read it.
+      mbar_init(&sm.empty[s], kPair ? 2 : 1);
       mbar_init(&sm.sf_ready[s], 1);
     }
     mbar_init(&sm.acc_full, 1);
@@ -312,10 +407,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // The peer's multicast loads and commits target this CTA's barriers.
+  if constexpr (kPair) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   const GroupTable& gt = sm.groups;
-  if (p.kind != 2) p.num_tiles = gt.tile0[p.G] * p.num_nt;
+  // Work items: tiles, or for CTA pairs pair-tiles walked by clusters.
+  const int rank = kPair ? static_cast<int>(cluster_rank()) : 0;
+  const int first = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int stride = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  if (kPair) {
+    p.num_tiles = p.kind != 2 ? gt.pair0[p.G] * p.num_nt : p.G * (p.N / BM / 2) * p.num_nt;
+  } else if (p.kind != 2) {
+    p.num_tiles = gt.tile0[p.G] * p.num_nt;
+  }
+  auto tile_of = [&](int t) { return kPair ? decode_pair(gt, p, t, rank) : decode(gt, p, t); };
 
   if (warp < EPI_WARP0) {
     regs_dec<88>();
@@ -325,8 +431,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int stage = 0;
         uint32_t phase = 0, issued = 0;
         bool alive = true;
-        for (int t = blockIdx.x; t < p.num_tiles && alive; t += gridDim.x) {
-          const Tile T = decode(gt, p, t);
+        for (int t = first; t < p.num_tiles && alive; t += stride) {
+          const Tile T = tile_of(t);
           const int nkb = num_kb(T);
           for (int kb = 0; kb < nkb; ++kb) {
             if (!mbar_wait(&sm.empty[stage], phase ^ 1u, ab, status)) {
@@ -336,10 +442,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int k0 = T.k_begin + kb * BK;
             mbar_arrive_expect_tx(&sm.full[stage], A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES);
             tma_load_2d(sm.a[stage], &tma_a, &sm.full[stage], k0, T.a_row0);
-            tma_load_2d(sm.b[stage], &tma_b, &sm.full[stage], k0, T.b_row0);
+            if constexpr (kPair) {
+              tma_load_2d_multicast(sm.b[stage] + rank * (B_BYTES / 2), &tma_b, &sm.full[stage], k0,
+                                    T.b_row0 + rank * (BN / 2), 0x3);
+            } else {
+              tma_load_2d(sm.b[stage], &tma_b, &sm.full[stage], k0, T.b_row0);
+            }
             bulk_load(sm.sfa[stage], ws_a + (T.sfa_chunk0 + kb * T.sfa_step) * BM, SFA_BYTES, &sm.full[stage]);
             bulk_load(sm.sfb[stage], ws_b + (T.sfb_chunk0 + kb * T.sfb_step) * BM, SFB_BYTES, &sm.full[stage]);
             ++issued;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if (kPair && alive) {
+          // The peer's last commits arrive on this CTA's empty barriers: wait
+          // for every stage's final release before the CTA may exit.
+          for (int i = 0; i < STAGES; ++i) {
+            if (!mbar_wait(&sm.empty[stage], phase ^ 1u, ab, status)) break;
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -372,8 +494,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint64_t a_desc0 = sdesc_kmajor_sw128(smem_u32(sm.a[0]));
         const uint64_t b_desc0 = sdesc_kmajor_sw128(smem_u32(sm.b[0]));
         const uint32_t acc = tmem + ACC_COL;
-        for (int t = blockIdx.x; t < p.num_tiles && alive; t += gridDim.x) {
-          const Tile T = decode(gt, p, t);
+        for (int t = first; t < p.num_tiles && alive; t += stride) {
+          const Tile T = tile_of(t);
           const int nkb = num_kb(T);
           if (nkb == 0) continue;  // empty WGRAD group: the epilogue writes zeros
           if (!mbar_wait(&sm.acc_empty, aphase ^ 1u, ab, status)) {
@@ -410,7 +532,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             sf_col + 4, (kb > 0 || j > 0) ? 1u : 0u);
               }
             }
-            mma_commit(&sm.empty[stage]);
+            if constexpr (kPair) mma_commit_multicast(&sm.empty[stage], 0x3);
+            else mma_commit(&sm.empty[stage]);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -434,8 +557,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool alive = true;
         const uint64_t sfa_desc0 = sdesc_plain_128b_rows(smem_u32(sm.sfa[0]));
         const uint64_t sfb_desc0 = sdesc_plain_128b_rows(smem_u32(sm.sfb[0]));
-        for (int t = blockIdx.x; t < p.num_tiles && alive; t += gridDim.x) {
-          const int nkb = num_kb(decode(gt, p, t));
+        for (int t = first; t < p.num_tiles && alive; t += stride) {
+          const int nkb = num_kb(tile_of(t));
           for (int kb = 0; kb < nkb; ++kb) {
             // Stage `stage` of this round has landed; its TMEM slot was last
             // read by the MMAs of the previous round, which completed before
@@ -476,8 +599,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
     const bool out32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
     uint32_t aphase = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      const Tile T = decode(gt, p, t);
+    for (int t = first; t < p.num_tiles; t += stride) {
+      const Tile T = tile_of(t);
       const int nkb = num_kb(T);
       const int out_row = T.out_row0 + row;
       const bool store = out_row < T.row_limit;
@@ -539,6 +662,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  // Neither CTA of a pair leaves while the other may still signal it.
+  if constexpr (kPair) cluster_sync_all();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -612,6 +737,35 @@ cudaError_t static_scratch_address(void** out) {
   return cudaSuccess;
 }
 
+// Clusters of two CTAs of the pair kernel that fit on the current device at
+// once, resolved on a device's first call (the query is not a stream
+// operation, so later calls can be captured in a CUDA graph).
+static cudaError_t pair_clusters(cudaLaunchConfig_t* cfg, int* out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static int clusters[kMaxDevices] = {};
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (clusters[dev] == 0) {
+    e = cudaFuncSetAttribute(mx_grouped_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    const dim3 grid = cfg->gridDim;
+    cfg->gridDim = dim3(2);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, mx_grouped_gemm_kernel<true>, cfg);
+    cfg->gridDim = grid;
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    clusters[dev] = n;
+  }
+  *out = clusters[dev];
+  return cudaSuccess;
+}
+
 size_t mx_grouped_gemm_workspace_bytes(int kind, int64_t G, int64_t M, int64_t N, int64_t K) {
   const Problem p = make_problem(kind, G, M, N, K);
   return align_up(static_cast<size_t>(packed_words_a(p)) * 4) + align_up(static_cast<size_t>(packed_words_b(p)) * 4);
@@ -631,8 +785,11 @@ cudaError_t launch_mx_grouped_gemm(const MxGroupedGemmArgs& g, cudaStream_t st) 
   uint32_t* ws_a = static_cast<uint32_t*>(g.workspace);
   uint32_t* ws_b = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(g.workspace) +
                                                align_up(static_cast<size_t>(packed_words_a(p)) * 4));
+  // CTA pairs sharing B: WGRAD pairs dW row tiles, so N / 128 must be even.
+  const bool pair = g.kind != 2 || (g.N / BM) % 2 == 0;
   CUtensorMap ta, tb;
-  if (!encode_kmajor_u8(&ta, g.a, a_rows, a_cols, BM) || !encode_kmajor_u8(&tb, g.b, b_rows, b_cols, BN))
+  if (!encode_kmajor_u8(&ta, g.a, a_rows, a_cols, BM) ||
+      !encode_kmajor_u8(&tb, g.b, b_rows, b_cols, pair ? BN / 2 : BN))
     return cudaErrorInvalidValue;
 
   const int64_t words = packed_words_a(p) + packed_words_b(p);
@@ -642,11 +799,36 @@ cudaError_t launch_mx_grouped_gemm(const MxGroupedGemmArgs& g, cudaStream_t st) 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  e = cudaFuncSetAttribute(mx_grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemBytes));
+  if (!pair) {
+    e = cudaFuncSetAttribute(mx_grouped_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    const int grid = p.num_tiles < g.num_sms ? p.num_tiles : g.num_sms;
+    mx_grouped_gemm_kernel<false><<<grid, NUM_THREADS, kSmemBytes, st>>>(ta, tb, ws_a, ws_b, g.group_end, g.out, p,
+                                                                          g.status);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  e = pair_clusters(&cfg, &clusters);
   if (e != cudaSuccess) return e;
-  const int grid = p.num_tiles < g.num_sms ? p.num_tiles : g.num_sms;
-  mx_grouped_gemm_kernel<<<grid, NUM_THREADS, kSmemBytes, st>>>(ta, tb, ws_a, ws_b, g.group_end, g.out, p, g.status);
+  // Pair-tiles: the kernel takes the exact count from group_end; this bounds it.
+  const int64_t pairs = g.kind == 2 ? p.G * (p.N / BM / 2) * p.num_nt : (p.mt_max / 2 + p.G) * p.num_nt;
+  const int64_t c = pairs < clusters ? pairs : clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * (c > 0 ? c : 1)));
+  e = cudaLaunchKernelEx(&cfg, mx_grouped_gemm_kernel<true>, ta, tb, static_cast<const uint32_t*>(ws_a),
+                         static_cast<const uint32_t*>(ws_b), g.group_end, g.out, p, g.status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -113,6 +113,38 @@ def test_grouped_random_layouts(seed):
     assert max(e) <= TOL, (G, M, K, N, list(sizes), e)
 
 
+@pytest.mark.parametrize("N,group_end", [(384, [96, 96, 320]), (640, [128, 160, 512])])
+def test_grouped_wgrad_odd_row_tiles(N, group_end):
+    # WGRAD with N / 128 odd: dW's 128-row tiles cannot be paired, so the
+    # unclustered kernel runs (every other shape pairs tiles that share B).
+    M, K = int(group_end[-1]), 256
+    G = len(group_end)
+    rng = np.random.default_rng(N)
+    x = inputs.normal_bf16(rng, (M, K), 1.0)
+    dy = inputs.normal_bf16(rng, (M, N), 1e-3)
+    xd, dyd = x.cuda(), dy.cuda()
+    ge = torch.from_numpy(np.asarray(group_end, np.int32)).cuda()
+    dyqT, dyeT = B.alloc_mx_col(dyd)
+    B.mxfp8_quant_1x32_col(dyd, dyqT, dyeT)
+    xqT, xeT = B.alloc_mx_col(xd)
+    B.mxfp8_quant_1x32_col(xd, xqT, xeT)
+    dW = torch.empty((G, N, K), dtype=torch.bfloat16, device="cuda")
+    ws = B.alloc_grouped_workspace(B.GROUPED_WGRAD, G, M, N, K, xd.device)
+    B.mxfp8_grouped_gemm(B.GROUPED_WGRAD, dyqT, dyeT, xqT, xeT, ge, G, M, N, K, dW, ws)
+    B.fp8bw_sync_status()
+    dWf, xf, dyf = f32(dW), f32(x), f32(dy)
+    starts = oracle.group_starts(np.asarray(group_end))
+    for g in range(G):
+        lo, hi = int(starts[g]), int(group_end[g])
+        if hi == lo:
+            assert np.all(dWf[g] == 0.0)
+            continue
+        a = oracle.mx_dequant_row(*oracle.mx_quant_1x32_col(np.ascontiguousarray(dyf[lo:hi]), oracle.RCEIL))
+        b = oracle.mx_dequant_row(*oracle.mx_quant_1x32_col(np.ascontiguousarray(xf[lo:hi]), oracle.RCEIL))
+        err = oracle.normalized_gemm_error(dWf[g], a @ b.T, oracle.row_norms(a), oracle.row_norms(b))
+        assert float(err.max()) <= TOL, (g, float(err.max()))
+
+
 def test_grouped_floor_mode():
     M, K, N, ge = 256, 256, 256, [64, 256]
     x, w, dy = moe_inputs(M, K, N, ge, seed=5)
