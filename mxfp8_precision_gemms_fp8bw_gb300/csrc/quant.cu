@@ -480,6 +480,40 @@ __global__ void __launch_bounds__(256, kQuantCtasPerSm)
   });
 }
 
+// 128x128 without the transposed copy: one CTA per tile, the tile loaded
+// straight into registers (thread (warp w, lane l) holds 16-byte chunk l % 16
+// of rows 16w + 2i + l / 16, i < 8: each half-warp reads one 256-byte row
+// segment), so the loads of every resident CTA are in flight at once and the
+// hardware balances tiles across SMs; the CTA's max is reduced through
+// shared memory.  Same arithmetic as quant_128x128_kernel.
+__global__ void __launch_bounds__(256) quant_128x128_direct_kernel(const uint16_t* __restrict__ x, int64_t C,
+                                                                   uint8_t* __restrict__ q, float* __restrict__ s,
+                                                                   int64_t s_ld) {
+  __shared__ float warp_max[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = lane >> 4, l16 = lane & 15;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128 + warp * 16 + h;
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * 128 + l16 * 8;
+  uint4 v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = ld_nc_v4(x + (r0 + 2 * i) * C + c);
+  uint32_t m = absmax8(v[0]);
+#pragma unroll
+  for (int i = 1; i < 8; ++i) m = absmax_bf16x2(m, absmax8(v[i]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = shfl_absmax(m, o);
+  if (lane == 0) warp_max[warp] = fmaxf(__uint_as_float((m & 0x7FFFu) << 16), __uint_as_float(m & 0x7FFF0000u));
+  __syncthreads();
+  float a = warp_max[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) a = fmaxf(a, warp_max[w]);
+  const float sc = blockwise_scale(a);
+  const float ny = neg_recip(sc);
+  if (threadIdx.x == 0) s[static_cast<int64_t>(blockIdx.y) * s_ld + blockIdx.x] = sc;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) st_v2(q + (r0 + 2 * i) * C + c, quant8_div(v[i], sc, ny));
+}
+
 // ---------------------------------------------------------------- MX 1x32 rowwise
 
 // CTA = 32 rows x 256 columns; warp w owns rows r0 + 4w + [0, 4); lane l
@@ -565,6 +599,11 @@ cudaError_t launch_quant_1x128_rowcol(const uint16_t* x, int64_t R, int64_t C, u
 
 cudaError_t launch_quant_128x128(const uint16_t* w, int64_t R, int64_t C, uint8_t* q, uint8_t* qT, float* s,
                                  int64_t s_ld, cudaStream_t st) {
+  if (qT == nullptr) {
+    quant_128x128_direct_kernel<<<dim3(static_cast<unsigned>(C / 128), static_cast<unsigned>(R / 128)), 256, 0, st>>>(
+        w, C, q, s, s_ld);
+    return finish();
+  }
   dim3 grid;
   if (!staged_grid((R / 128) * (C / 128), grid)) return cudaErrorInvalidConfiguration;
   quant_128x128_kernel<<<grid, 256, kQuantSmem, st>>>(w, R, C, q, qT, s, s_ld);
