@@ -183,13 +183,18 @@ def test_full_size_dense_row_and_col_quant(dense):
 
 
 def test_full_size_dense_weight_quant(dense):
+    # Both kernels: the staged one (with q^T) and the register-staged one
+    # that runs when no q^T is asked for (the linear layer's case).
     q, qT, s = run_128(dense.w)
+    q2, _, s2 = run_128(dense.w, with_t=False)
     wf = f32(dense.w)
     for r0, r1 in _chunks(wf.shape[0], 2048):
         qo, qTo, so = oracle.quant_128x128(np.ascontiguousarray(wf[r0:r1]))
         assert np.array_equal(q[r0:r1], qo)
         assert np.array_equal(qT[:, r0:r1], qTo)
         assert np.array_equal(bits(s[r0 // 128:r1 // 128, :so.shape[1]]), bits(so))
+        assert np.array_equal(q2[r0:r1], qo)
+        assert np.array_equal(bits(s2[r0 // 128:r1 // 128, :so.shape[1]]), bits(so))
 
 
 @pytest.fixture(scope="module")
