@@ -466,8 +466,9 @@ def kernel_table(per, algo, fp8_peak, hbm_peak):
 
 def run_moe(dev, steps, warmup, fp8_peak, hbm_peak, world, dense: bool = False):
     """The MXFP8 MoE grouped linear step (M=16384 tokens over 8 experts,
-    K=5120, N=8192): nine launches, timed like the dense step.  With
-    dense=True, the MXFP8 dense linear instead: the same nine calls with one
+    K=5120, N=8192): six library calls (three fused row + column MX
+    quantizations and three grouped GEMMs), timed like the dense step.  With
+    dense=True, the MXFP8 dense linear instead: the same six calls with one
     group on the dense workload's x, W, dy (M=16384, K=5120, N=8192)."""
     import torch
 
@@ -514,7 +515,7 @@ def run_moe(dev, steps, warmup, fp8_peak, hbm_peak, world, dense: bool = False):
                      "unit": "TFLOP/s", "frac": round(dom_ach / fp8_peak, 4),
                      "traffic": load_traffic(("mxfp8_dense/" if dense else "") + dom)},
         "kernels": kernel_table(per, algo, fp8_peak, hbm_peak),
-        "linear_us": linear_us(per, ["mx_quant_1x32_row(x)", "mx_quant_1x32_row(W)", "mx_grouped_fwd"]),
+        "linear_us": linear_us(per, ["mx_quant_1x32_rowcol(x)", "mx_quant_1x32_rowcol(W)", "mx_grouped_fwd"]),
     }
 
 
@@ -717,8 +718,10 @@ def run_dense_table(dev, steps, warmup):
 
 def run_moe_table(dev, steps, warmup):
     """The MXFP8 grouped linear over the shapes of PR #3037's microbenchmark
-    table, in its columns: forward (quantizations + grouped GEMM) and forward
-    + backward (the whole nine-call step) in microseconds.  One JSON line per
+    table, in its columns: forward (the fused row + column quantizations of x
+    and W, which also produce the backward's colwise operands, and the
+    grouped GEMM) and forward + backward (the whole six-call step) in
+    microseconds.  One JSON line per
     shape; inputs are seeded N(0,1) / N(0,0.02) / N(0,1e-3) draws made on the
     device (timing only, no parity check), token groups of multiples of 32."""
     import torch
@@ -742,7 +745,7 @@ def run_moe_table(dev, steps, warmup):
             B.fp8bw_sync_status()
             ms, per = time_kernels(kern, steps, torch.cuda.current_stream(dev))
             B.fp8bw_sync_status()
-            lu = linear_us(per, ["mx_quant_1x32_row(x)", "mx_quant_1x32_row(W)", "mx_grouped_fwd"])
+            lu = linear_us(per, ["mx_quant_1x32_rowcol(x)", "mx_quant_1x32_rowcol(W)", "mx_grouped_fwd"])
             print(json.dumps({"table": "mxfp8_grouped_mm", "M": M, "N": N, "K": K, "G": G, **lu,
                               "fwd_bwd_tflops": round(6 * M * N * K / (lu["fwd_bwd_us"] * 1e-6) / 1e12, 1)}),
                   flush=True)

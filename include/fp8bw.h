@@ -234,6 +234,23 @@ int mxfp8_quant_1x32_col(const fp8bw_bf16* x, int64_t R, int64_t C,
 int mxfp8_quant_3d_col(const fp8bw_bf16* w, int64_t G, int64_t N, int64_t K,
                        uint8_t* qT, uint8_t* e8, int mode, void* stream);
 
+/* Both MX quantizations of G stacked matrices x [G, R, C] from one read of
+ * x: the rowwise one (1x32 blocks along C) and the colwise one (32-row
+ * blocks along R, written transposed per matrix).  Byte-identical to
+ * mxfp8_quant_1x32_row on x viewed as [G*R, C] plus mxfp8_quant_1x32_col of
+ * each matrix (G = 1: a 2D operand such as x or dy of the MoE step) or
+ * mxfp8_quant_3d_col (G experts: W as [G, N, K], R = N, C = K).  On the
+ * pages the 3D colwise quantization is a kernel of its own ([PR3037]
+ * Summary: the new CUDA kernel in the grouped-mm backward); reading the
+ * input once for both outputs is performance work, not a step the pages
+ * define.
+ *   x   : bf16 [G, R, C]
+ *   q   : e4m3 [G*R, C]        e8  : E8M0 [G*R][C/32]
+ *   qT  : e4m3 [G, C, R]       e8T : E8M0 [G][C][R/32]
+ * G >= 1; R and C positive multiples of 32. */
+int mxfp8_quant_1x32_rowcol(const fp8bw_bf16* x, int64_t G, int64_t R, int64_t C, uint8_t* q, uint8_t* e8,
+                            uint8_t* qT, uint8_t* e8T, int mode, void* stream);
+
 enum fp8bw_grouped_kind { FP8BW_GROUPED_FWD = 0, FP8BW_GROUPED_DGRAD = 1, FP8BW_GROUPED_WGRAD = 2 };
 
 /* MoE grouped GEMM on MXFP8 operands ([PR3037] Microbenchmarks: grouped mm

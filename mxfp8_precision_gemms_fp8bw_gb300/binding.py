@@ -41,6 +41,7 @@ _SIGNATURES = {
     "mxfp8_quant_1x32_row": [_P, _I64, _I64, _P, _P, _INT, _P],
     "mxfp8_quant_1x32_col": [_P, _I64, _I64, _P, _P, _INT, _P],
     "mxfp8_quant_3d_col": [_P, _I64, _I64, _I64, _P, _P, _INT, _P],
+    "mxfp8_quant_1x32_rowcol": [_P, _I64, _I64, _I64, _P, _P, _P, _P, _INT, _P],
     "mxfp8_grouped_gemm": [_INT, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, ctypes.c_size_t, _P],
     "mxfp8_grouped_gemm_workspace_bytes": [_INT, _I64, _I64, _I64, _I64],
     "mxfp8_grouped_gemm_noalloc": [_INT, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P],
@@ -156,6 +157,15 @@ def mxfp8_quant_3d_col(w, qT, e8, mode=MX_RCEIL, stream=None) -> None:
     G, N, K = w.shape
     _check(lib().mxfp8_quant_3d_col(_ptr(w, _BF16, "w"), G, N, K, _ptr(qT, _U8, "qT"), _ptr(e8, _U8, "e8"), mode,
                                     _stream(stream)))
+
+
+def mxfp8_quant_1x32_rowcol(x, q, e8, qT, e8T, mode=MX_RCEIL, stream=None) -> None:
+    """Both MX quantizations of x [R, C] (G = 1) or of G stacked matrices
+    x [G, R, C] from one read: q [G*R, C] / e8 [G*R, C/32] rowwise and
+    qT [G, C, R] / e8T [G, C, R/32] colwise (qT [C, R], e8T [C, R/32] for 2D x)."""
+    G, R, C = (1, *x.shape) if x.dim() == 2 else x.shape
+    _check(lib().mxfp8_quant_1x32_rowcol(_ptr(x, _BF16, "x"), G, R, C, _ptr(q, _U8, "q"), _ptr(e8, _U8, "e8"),
+                                         _ptr(qT, _U8, "qT"), _ptr(e8T, _U8, "e8T"), mode, _stream(stream)))
 
 
 # ------------------------------------------------------------------ GEMMs

@@ -232,6 +232,27 @@ FP8BW_API int mxfp8_quant_3d_col(const fp8bw_bf16* w, int64_t G, int64_t N, int6
   return mx_col_common("mxfp8_quant_3d_col", w, G, N, K, qT, e8, mode, stream);
 }
 
+FP8BW_API int mxfp8_quant_1x32_rowcol(const fp8bw_bf16* x, int64_t G, int64_t R, int64_t C, uint8_t* q, uint8_t* e8,
+                                      uint8_t* qT, uint8_t* e8T, int mode, void* stream) {
+  const char* name = "mxfp8_quant_1x32_rowcol";
+  if (!x || !q || !e8 || !qT || !e8T) return fail(FP8BW_ERR_NULL, "%s: x, q, e8, qT and e8T must be non-NULL", name);
+  if (!dim_ok(G, 1) || G > 65535 || !dim_ok(R, 32) || !dim_ok(C, 32) || (R + 127) / 128 > 65535)
+    return fail(FP8BW_ERR_SHAPE, "%s: G=%lld must be positive, R=%lld and C=%lld positive multiples of 32", name,
+                (long long)G, (long long)R, (long long)C);
+  if (!aligned16(x) || !aligned16(q) || !aligned16(e8) || !aligned16(qT) || !aligned16(e8T))
+    return fail(FP8BW_ERR_ALIGN, "%s: pointers must be 16-byte aligned", name);
+  if (mode != FP8BW_MX_RCEIL && mode != FP8BW_MX_FLOOR)
+    return fail(FP8BW_ERR_ARG, "%s: mode %d is neither RCEIL (0) nor FLOOR (1)", name, mode);
+  const int64_t n = G * R * C;
+  if (overlaps(x, n * 2, q, n) || overlaps(x, n * 2, qT, n) || overlaps(q, n, qT, n) || overlaps(x, n * 2, e8, n / 32) ||
+      overlaps(x, n * 2, e8T, n / 32) || overlaps(e8, n / 32, e8T, n / 32) || overlaps(q, n, e8T, n / 32) ||
+      overlaps(qT, n, e8, n / 32))
+    return fail(FP8BW_ERR_LAYOUT, "%s: outputs overlap the input or each other", name);
+  DeviceState* d;
+  if (int rc = current_device(&d)) return rc;
+  return launched(fp8bw::launch_mx_quant_rowcol(x, G, R, C, q, e8, qT, e8T, mode, as_stream(stream)), name);
+}
+
 // ============================================================ blockwise GEMMs
 
 static int gemm_common(const char* name, fp8bw::BlockwiseGemmArgs& g, void* stream) {

@@ -19,6 +19,8 @@ cudaError_t launch_mx_quant_row(const uint16_t* x, int64_t R, int64_t C, uint8_t
                                 cudaStream_t st);
 cudaError_t launch_mx_quant_col(const uint16_t* x, int64_t G, int64_t R, int64_t C, uint8_t* qT, uint8_t* e8,
                                 int mode, cudaStream_t st);
+cudaError_t launch_mx_quant_rowcol(const uint16_t* x, int64_t G, int64_t R, int64_t C, uint8_t* q, uint8_t* e8,
+                                   uint8_t* qT, uint8_t* e8T, int mode, cudaStream_t st);
 
 // Which operand-B scale structure a blockwise GEMM applies (see gemm_blockwise.cu).
 enum class BScale : int {

@@ -422,6 +422,43 @@ __global__ void __launch_bounds__(256, kQuantCtasPerSm)
   });
 }
 
+// Rowwise MX (1x32 along the columns) of the staged tile's rows, in the
+// mapping of read_rows: a 32-column block spans the 4 lanes that hold its
+// chunks, which reduce its max with two shuffles.  Same arithmetic as
+// mx_quant_row_kernel.
+__device__ __forceinline__ void rowwise_mx_from_tile(const StagedTile& t, int64_t R, int64_t C, int64_t r0, int64_t c0,
+                                                     uint8_t* __restrict__ q, uint8_t* __restrict__ e8, int mode) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = lane >> 4, l16 = lane & 15;
+  const int64_t col = c0 + l16 * 8;
+  uint4 v[8];
+  read_rows(t, v);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t r = r0 + warp * 16 + i * 2 + h;
+    const uint32_t mm = shfl_absmax(shfl_absmax(absmax8(v[i]), 1), 2);
+    const float a = fmaxf(__uint_as_float((mm & 0x7FFFu) << 16), __uint_as_float(mm & 0x7FFF0000u));
+    if (r >= R || col >= C) continue;  // C % 32 == 0: a 32-column block is all in or all out
+    const int E = mx_exponent(a, mode);
+    st_v2(q + r * C + col, quant8_mul(v[i], pow2_neg(E)));
+    if ((l16 & 3) == 0) e8[r * (C / 32) + col / 32] = static_cast<uint8_t>(E + 127);
+  }
+}
+
+// Both MX quantizations of G stacked matrices [R, C] from one read: rowwise
+// (1x32 along C) into q [G*R, C], e8 [G*R][C/32] and colwise (32 along R)
+// into qT [G, C, R], e8T [G][C][R/32].
+__global__ void __launch_bounds__(256, kQuantCtasPerSm)
+    mx_quant_rowcol_kernel(const uint16_t* __restrict__ x, int64_t G, int64_t R, int64_t C, uint8_t* __restrict__ q,
+                           uint8_t* __restrict__ e8, uint8_t* __restrict__ qT, uint8_t* __restrict__ e8T, int mode) {
+  extern __shared__ __align__(128) uint8_t quant_smem[];
+  StagedTile* ring = reinterpret_cast<StagedTile*>(quant_smem);
+  for_each_staged_tile(x, tile_space(G, R, C), ring, [&](const StagedTile& t, int64_t g, int64_t r0, int64_t c0) {
+    rowwise_mx_from_tile(t, R, C, r0, c0, q + g * R * C, e8 + g * R * (C / 32), mode);
+    colwise_from_tile<true>(t, R, C, r0, c0, qT + g * R * C, nullptr, e8T + g * C * (R / 32), mode);
+  });
+}
+
 // G stacked matrices (the 3D expert case; G = 1 for a plain 2D operand).
 __global__ void __launch_bounds__(256, kQuantCtasPerSm)
     mx_quant_col_kernel(const uint16_t* __restrict__ x, int64_t G, int64_t R, int64_t C, uint8_t* __restrict__ qT,
@@ -562,6 +599,7 @@ static int staged_grid_cap() {
     if (cudaFuncSetAttribute(quant_1x128_col_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ||
         cudaFuncSetAttribute(quant_1x128_rowcol_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ||
         cudaFuncSetAttribute(mx_quant_col_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ||
+        cudaFuncSetAttribute(mx_quant_rowcol_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ||
         cudaFuncSetAttribute(quant_128x128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))
       return 0;
     sms[dev] = n;
@@ -622,6 +660,14 @@ cudaError_t launch_mx_quant_col(const uint16_t* x, int64_t G, int64_t R, int64_t
   dim3 grid;
   if (!staged_grid(G * ((R + 127) / 128) * ((C + 127) / 128), grid)) return cudaErrorInvalidConfiguration;
   mx_quant_col_kernel<<<grid, 256, kQuantSmem, st>>>(x, G, R, C, qT, e8, mode);
+  return finish();
+}
+
+cudaError_t launch_mx_quant_rowcol(const uint16_t* x, int64_t G, int64_t R, int64_t C, uint8_t* q, uint8_t* e8,
+                                   uint8_t* qT, uint8_t* e8T, int mode, cudaStream_t st) {
+  dim3 grid;
+  if (!staged_grid(G * ((R + 127) / 128) * ((C + 127) / 128), grid)) return cudaErrorInvalidConfiguration;
+  mx_quant_rowcol_kernel<<<grid, 256, kQuantSmem, st>>>(x, G, R, C, q, e8, qT, e8T, mode);
   return finish();
 }
 

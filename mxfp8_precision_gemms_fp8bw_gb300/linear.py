@@ -120,11 +120,12 @@ class MxExpertWeights:
 
 
 def mx_quantize_experts(w: torch.Tensor, mode: int = B.MX_RCEIL, stream=None) -> MxExpertWeights:
+    """Rowwise (forward) and 3D colwise (dgrad) MX codes of the expert
+    weights w [G, N, K], both from one read of w."""
     G, N, K = w.shape
     q, e8 = B.alloc_mx_row(w.view(G * N, K))
-    B.mxfp8_quant_1x32_row(w.view(G * N, K), q, e8, mode, stream)
     qT, e8c = B.alloc_mx_3d_col(w)
-    B.mxfp8_quant_3d_col(w, qT, e8c, mode, stream)
+    B.mxfp8_quant_1x32_rowcol(w, q, e8, qT, e8c, mode, stream)
     return MxExpertWeights(q.view(G, N, K), e8, qT, e8c)
 
 
@@ -144,13 +145,13 @@ def mx_moe_backward(dy: torch.Tensor, x: torch.Tensor, wq: MxExpertWeights, grou
     M, N = dy.shape
     K = x.shape[1]
     G = wq.q_row.shape[0]
+    # dy rowwise (dgrad) and colwise (wgrad) from one read of dy.
     dyq, dye = B.alloc_mx_row(dy)
-    B.mxfp8_quant_1x32_row(dy, dyq, dye, mode, stream)
+    dyqT, dyeT = B.alloc_mx_col(dy)
+    B.mxfp8_quant_1x32_rowcol(dy, dyq, dye, dyqT, dyeT, mode, stream)
     dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device)
     ws = B.alloc_grouped_workspace(B.GROUPED_DGRAD, G, M, N, K, dy.device)
     B.mxfp8_grouped_gemm(B.GROUPED_DGRAD, dyq, dye, wq.qT_col, wq.e8_col, group_end, G, M, N, K, dx, ws, stream)
-    dyqT, dyeT = B.alloc_mx_col(dy)
-    B.mxfp8_quant_1x32_col(dy, dyqT, dyeT, mode, stream)
     xqT, xeT = B.alloc_mx_col(x)
     B.mxfp8_quant_1x32_col(x, xqT, xeT, mode, stream)
     dW = torch.empty((G, N, K), dtype=torch.bfloat16, device=dy.device)
@@ -227,7 +228,8 @@ class MxMoEWorkspace:
     """Every output of one MXFP8 MoE grouped linear forward+backward, allocated once.
 
     Inputs: x [M, K], w [G, N, K], dy [M, N] bf16 and group_end int32 [G] on
-    the workspace's device.  ``kernels`` lists the step's nine library calls.
+    the workspace's device.  ``kernels`` lists the step's six library calls:
+    each of x, W and dy is read once for both its MX quantizations.
     """
 
     def __init__(self, M: int, N: int, K: int, G: int, device="cuda", mode: int = B.MX_RCEIL):
@@ -247,18 +249,17 @@ class MxMoEWorkspace:
 
     def kernels(self, x, w, dy, group_end, stream=None):
         M, N, K, G, md = self.M, self.N, self.K, self.G, self.mode
-        w2 = w.view(G * N, K)
         return [
-            ("mx_quant_1x32_row(x)", lambda: B.mxfp8_quant_1x32_row(x, self.xq, self.xe, md, stream)),
-            ("mx_quant_1x32_row(W)", lambda: B.mxfp8_quant_1x32_row(w2, self.wq, self.we, md, stream)),
-            ("mx_quant_3d_col(W)", lambda: B.mxfp8_quant_3d_col(w, self.wqT, self.weT, md, stream)),
+            ("mx_quant_1x32_rowcol(x)", lambda: B.mxfp8_quant_1x32_rowcol(x, self.xq, self.xe, self.xqT, self.xeT,
+                                                                          md, stream)),
+            ("mx_quant_1x32_rowcol(W)", lambda: B.mxfp8_quant_1x32_rowcol(w, self.wq, self.we, self.wqT, self.weT,
+                                                                          md, stream)),
             ("mx_grouped_fwd", lambda: B.mxfp8_grouped_gemm(B.GROUPED_FWD, self.xq, self.xe, self.wq, self.we,
                                                             group_end, G, M, N, K, self.y, self.ws, stream)),
-            ("mx_quant_1x32_row(dy)", lambda: B.mxfp8_quant_1x32_row(dy, self.dyq, self.dye, md, stream)),
+            ("mx_quant_1x32_rowcol(dy)", lambda: B.mxfp8_quant_1x32_rowcol(dy, self.dyq, self.dye, self.dyqT,
+                                                                           self.dyeT, md, stream)),
             ("mx_grouped_dgrad", lambda: B.mxfp8_grouped_gemm(B.GROUPED_DGRAD, self.dyq, self.dye, self.wqT,
                                                               self.weT, group_end, G, M, N, K, self.dx, self.ws, stream)),
-            ("mx_quant_1x32_col(dy)", lambda: B.mxfp8_quant_1x32_col(dy, self.dyqT, self.dyeT, md, stream)),
-            ("mx_quant_1x32_col(x)", lambda: B.mxfp8_quant_1x32_col(x, self.xqT, self.xeT, md, stream)),
             ("mx_grouped_wgrad", lambda: B.mxfp8_grouped_gemm(B.GROUPED_WGRAD, self.dyqT, self.dyeT, self.xqT,
                                                               self.xeT, group_end, G, M, N, K, self.dW, self.ws, stream)),
         ]
@@ -270,16 +271,14 @@ class MxMoEWorkspace:
 
     def algorithmic(self):
         M, N, K, G = self.M, self.N, self.K, self.G
-        mx = lambda r, c: r * c * 3 + r * c // 32  # noqa: E731  bf16 in, e4m3 out, one byte per 32
+        # bf16 in once; e4m3 out twice (rowwise and colwise); one E8M0 byte per 32 each way
+        mx2 = lambda r, c: r * c * 4 + 2 * (r * c // 32)  # noqa: E731
         return {
-            "mx_quant_1x32_row(x)": ("bytes", mx(M, K)),
-            "mx_quant_1x32_row(W)": ("bytes", mx(G * N, K)),
-            "mx_quant_3d_col(W)": ("bytes", mx(G * N, K)),
+            "mx_quant_1x32_rowcol(x)": ("bytes", mx2(M, K)),
+            "mx_quant_1x32_rowcol(W)": ("bytes", mx2(G * N, K)),
             "mx_grouped_fwd": ("flops", 2 * M * N * K),
-            "mx_quant_1x32_row(dy)": ("bytes", mx(M, N)),
+            "mx_quant_1x32_rowcol(dy)": ("bytes", mx2(M, N)),
             "mx_grouped_dgrad": ("flops", 2 * M * N * K),
-            "mx_quant_1x32_col(dy)": ("bytes", mx(M, N)),
-            "mx_quant_1x32_col(x)": ("bytes", mx(M, K)),
             "mx_grouped_wgrad": ("flops", 2 * M * N * K),
         }
 

@@ -30,7 +30,8 @@ def test_header_declares_the_abi():
         "fp8bw_quant_1x128_row", "fp8bw_quant_1x128_col", "fp8bw_quant_128x128", "fp8bw_quant_1x128_rowcol",
         "fp8bw_gemm_fwd", "fp8bw_gemm_fwd_quant", "fp8bw_gemm_dgrad", "fp8bw_gemm_wgrad", "fp8bw_gemm_wgrad_acc_f32",
         "fp8bw_gemm_wgrad_ws", "fp8bw_gemm_wgrad_workspace_bytes",
-        "mxfp8_quant_1x32_row", "mxfp8_quant_1x32_col", "mxfp8_quant_3d_col", "mxfp8_grouped_gemm",
+        "mxfp8_quant_1x32_row", "mxfp8_quant_1x32_col", "mxfp8_quant_3d_col", "mxfp8_quant_1x32_rowcol",
+        "mxfp8_grouped_gemm",
         "mxfp8_grouped_gemm_workspace_bytes", "mxfp8_grouped_gemm_noalloc",
         "fp8bw_sync_status", "fp8bw_last_error", "fp8bw_selftest_bounded_wait",
     ])
@@ -172,3 +173,18 @@ def test_noalloc_rejects_dims_beyond_its_scratch(L):
     rc = L.mxfp8_grouped_gemm_noalloc(1, P, 2 * P, 3 * P, 4 * P, 5 * P, 8, 16384, 16384, 16384, 64 * P, None)
     assert rc == binding.ERR_SHAPE
     assert "scratch" in binding.last_error()
+
+
+def test_mx_rowcol_validation(L):
+    # x [G=2, R=64, C=64] bf16 at P; q at 64P, e8 at 80P, qT at 96P, e8T at 112P
+    args = (P, 2, 64, 64, 64 * P, 80 * P, 96 * P, 112 * P)
+    assert L.mxfp8_quant_1x32_rowcol(P, 2, 64, 64, 64 * P, 80 * P, None, 112 * P, 0, None) == binding.ERR_NULL
+    assert L.mxfp8_quant_1x32_rowcol(P, 2, 48, 64, 64 * P, 80 * P, 96 * P, 112 * P, 0, None) == binding.ERR_SHAPE
+    assert L.mxfp8_quant_1x32_rowcol(P, 2, 64, 40, 64 * P, 80 * P, 96 * P, 112 * P, 0, None) == binding.ERR_SHAPE
+    assert L.mxfp8_quant_1x32_rowcol(P, 0, 64, 64, 64 * P, 80 * P, 96 * P, 112 * P, 0, None) == binding.ERR_SHAPE
+    assert L.mxfp8_quant_1x32_rowcol(P, 2, 64, 64, 64 * P, 80 * P + 4, 96 * P, 112 * P, 0, None) == binding.ERR_ALIGN
+    assert L.mxfp8_quant_1x32_rowcol(*args, 2, None) == binding.ERR_ARG
+    # qT overlapping q (8 KB of codes from 64P)
+    assert L.mxfp8_quant_1x32_rowcol(P, 2, 64, 64, 64 * P, 80 * P, 64 * P + 4096, 112 * P, 0, None) == binding.ERR_LAYOUT
+    # e8 overlapping x (16 KB of bf16 from P)
+    assert L.mxfp8_quant_1x32_rowcol(P, 2, 64, 64, 64 * P, P + 1024, 96 * P, 112 * P, 0, None) == binding.ERR_LAYOUT

@@ -147,6 +147,45 @@ def test_mx_3d_col_bit_exact(mode):
     assert np.array_equal(u8(e8), eo)
 
 
+def _mx_rowcol(x, mode):
+    """Both MX quantizations of x ([R, C] or [G, R, C]) from the fused kernel."""
+    xd = x.cuda()
+    G, R, C = (1, *x.shape) if x.dim() == 2 else x.shape
+    q = torch.empty((G * R, C), dtype=torch.uint8, device="cuda")
+    e8 = torch.empty((G * R, C // 32), dtype=torch.uint8, device="cuda")
+    qT = torch.empty((G, C, R), dtype=torch.uint8, device="cuda")
+    e8T = torch.empty((G, C, R // 32), dtype=torch.uint8, device="cuda")
+    B.mxfp8_quant_1x32_rowcol(xd, q, e8, qT, e8T, mode)
+    B.fp8bw_sync_status()
+    return u8(q), u8(e8), u8(qT), u8(e8T)
+
+
+@pytest.mark.parametrize("mode", [B.MX_RCEIL, B.MX_FLOOR])
+@pytest.mark.parametrize("R,C,seed", [(32, 32, 20), (96, 160, 21), (288, 544, 22), (544, 256, 23)])
+def test_mx_rowcol_bit_exact(mode, R, C, seed):
+    # The fused kernel against both oracle quantizers, on blocks adversarial
+    # along the rows (rowwise pass) and along the columns (colwise pass).
+    for x in (adversarial_bf16(R, C, seed, block=32), transpose_adversarial(R, C, seed, block=32)):
+        q, e8, qT, e8T = _mx_rowcol(x, mode)
+        qo, eo = oracle.mx_quant_1x32_row(f32(x), mode)
+        qTo, eTo = oracle.mx_quant_1x32_col(f32(x), mode)
+        assert np.array_equal(q, qo) and np.array_equal(e8, eo)
+        assert np.array_equal(qT[0], qTo) and np.array_equal(e8T[0], eTo)
+
+
+@pytest.mark.parametrize("mode", [B.MX_RCEIL, B.MX_FLOOR])
+def test_mx_rowcol_3d_bit_exact(mode):
+    # Stacked expert weights [G, N, K]: rowwise along K over [G*N, K], and the
+    # 3D colwise (32 along N per expert, written [G, K, N]).
+    G, N, K = 3, 160, 288
+    w = torch.stack([transpose_adversarial(N, K, 30 + g, block=32) for g in range(G)])
+    q, e8, qT, e8T = _mx_rowcol(w, mode)
+    qo, eo = oracle.mx_quant_1x32_row(f32(w).reshape(G * N, K), mode)
+    qTo, eTo = oracle.mx_quant_3d_col(f32(w), mode)
+    assert np.array_equal(q, qo) and np.array_equal(e8, eo)
+    assert np.array_equal(qT, qTo) and np.array_equal(e8T, eTo)
+
+
 # ---------------------------------------------------------------- full size
 
 @pytest.fixture(scope="module")
@@ -224,19 +263,26 @@ def test_full_size_moe_mx_quant_bit_exact(moe_tensors, name):
     # oracle: rowwise (1x32 along the last dim) for x, dy and W viewed as
     # [G*N, K]; colwise (32 rows, written transposed) for x and dy; 3D colwise
     # (32 along N per expert, written [G, K, N]) for W.  Both sides in RCEIL.
+    # The fused row + column kernel (the MoE step's path) is checked against
+    # the same oracle bytes.
     t = getattr(moe_tensors, name)
     R2 = t.reshape(-1, t.shape[-1])
     q, e = _mx_gpu("row", R2)
+    fq, fe, fqT, feT = _mx_rowcol(t, B.MX_RCEIL)
     host = f32(R2)
     chunks = [(np.ascontiguousarray(host[r0:r1]),) for r0, r1 in _chunks(host.shape[0], 2048)]
     for (r0, r1), (qo, eo) in zip(_chunks(host.shape[0], 2048), oracle_map("mx_quant_1x32_row", chunks)):
         assert np.array_equal(q[r0:r1], qo), (name, "row", r0)
         assert np.array_equal(e[r0:r1], eo), (name, "row e8", r0)
+        assert np.array_equal(fq[r0:r1], qo), (name, "fused row", r0)
+        assert np.array_equal(fe[r0:r1], eo), (name, "fused row e8", r0)
     if name != "w":
         qT, eT = _mx_gpu("col", t)
         for (r0, r1), (qo, eo) in zip(_chunks(host.shape[0], 2048), oracle_map("mx_quant_1x32_col", chunks)):
             assert np.array_equal(qT[:, r0:r1], qo), (name, "col", r0)
             assert np.array_equal(eT[:, r0 // 32:r1 // 32], eo), (name, "col e8", r0)
+            assert np.array_equal(fqT[0][:, r0:r1], qo), (name, "fused col", r0)
+            assert np.array_equal(feT[0][:, r0 // 32:r1 // 32], eo), (name, "fused col e8", r0)
     else:
         G, N, K = t.shape
         qT, eT = _mx_gpu("3d", t)
@@ -246,6 +292,8 @@ def test_full_size_moe_mx_quant_bit_exact(moe_tensors, name):
         for (g, n0, n1), (qo, eo) in zip(spans, results):
             assert np.array_equal(qT[g][:, n0:n1], qo), ("w", "3d", g, n0)
             assert np.array_equal(eT[g][:, n0 // 32:n1 // 32], eo), ("w", "3d e8", g, n0)
+            assert np.array_equal(fqT[g][:, n0:n1], qo), ("w", "fused 3d", g, n0)
+            assert np.array_equal(feT[g][:, n0 // 32:n1 // 32], eo), ("w", "fused 3d e8", g, n0)
 
 
 def test_selftest_bounded_wait_reports_timeout():
