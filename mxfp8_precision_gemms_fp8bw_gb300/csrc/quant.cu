@@ -21,25 +21,31 @@ namespace fp8bw {
 
 // ---------------------------------------------------------------- scale rules
 
-// MXFP8 rule: unbiased E8M0 exponent of a block from its amax.
+// MXFP8 rule: unbiased E8M0 exponent E of a block from its amax.
 //   RCEIL: smallest E with 448 * 2^E >= amax.  With amax = 1.m * 2^e and
 //          448 = 1.75 * 2^8 this is e - 8, plus one when 1.m > 1.75.
 //   FLOOR: floor(log2 amax) - 8 = e - 8.
 // Clamped to [-127, 127]; zero and subnormal amax give -127.
-__device__ __forceinline__ int mx_exponent(float amax, int mode) {
-  const uint32_t b = __float_as_uint(amax);
-  const int ef = static_cast<int>((b >> 23) & 0xFF);
-  if (ef == 0) return -127;
-  int E = ef - 127 - 8;
-  if (mode == 0 && (b & 0x7FFFFFu) > 0x600000u) E += 1;
-  return max(-127, min(127, E));
+//
+// Every block max here is an exact bf16 value, taken as its magnitude bits
+// A = (ef << 7) | m (8-bit biased exponent, 7-bit mantissa).  RCEIL's "plus
+// one when 1.m > 1.75" (m > 0x60) is then the carry out of m + 0x1F, so
+//   t = (A + round) >> 7,  round = 0x1F (RCEIL) or 0 (FLOOR),
+// is E + 135.  The clamp E >= -127 is t >= 8 (it also catches ef = 0); the
+// top clamp cannot bind (t <= 256).  The E8M0 byte E + 127 is t - 8 and the
+// scale 2^-E has biased exponent 262 - t, in [6, 254]: always a normal float.
+struct MxScale {
+  uint32_t e8;  // the E8M0 code E + 127
+  float mul;    // 2^-E
+};
+__device__ __forceinline__ uint32_t mx_round(int mode) { return mode == 0 ? 0x1Fu : 0u; }
+__device__ __forceinline__ MxScale mx_scale(uint32_t A, uint32_t round) {
+  const uint32_t t = max((A + round) >> 7, 8u);
+  return MxScale{t - 8u, __uint_as_float((262u - t) << 23)};
 }
-
-// 2^-E as a float for E in [-127, 127] (exact; 2^-127 is subnormal).
-__device__ __forceinline__ float pow2_neg(int E) {
-  const int be = 127 - E;  // biased exponent of 2^-E
-  return be > 0 ? __uint_as_float(static_cast<uint32_t>(be) << 23) : __uint_as_float(0x00400000u);
-}
+// Magnitude bits of the larger of the two bf16 values packed in `w` (the
+// sign bits may be anything).
+__device__ __forceinline__ uint32_t bf16_pair_max_bits(uint32_t w) { return max(w & 0x7FFFu, (w >> 16) & 0x7FFFu); }
 
 // max(|a|, |b|) in each bf16 half (exact); the result's sign bits are
 // meaningless (max.xorsign.abs sets them to the XOR of the inputs' signs).
@@ -70,6 +76,11 @@ __device__ __forceinline__ uint32_t shfl_absmax(uint32_t m, int lane_mask) {
 __device__ __forceinline__ float unpack_amax(const uint32_t (&m)[4], int c) {
   const uint32_t w = (c & 4) ? ((c & 2) ? m[3] : m[2]) : ((c & 2) ? m[1] : m[0]);
   return __uint_as_float((c & 1) ? (w & 0x7FFF0000u) : (w & 0x7FFFu) << 16);
+}
+// The same value as bf16 magnitude bits (c a compile-time constant).
+__device__ __forceinline__ uint32_t unpack_amax_bits(const uint32_t (&m)[4], int c) {
+  const uint32_t w = m[c >> 1];
+  return (c & 1) ? (w >> 16) & 0x7FFFu : w & 0x7FFFu;
 }
 
 // Element j (0..7) of 8 packed bf16.
@@ -367,11 +378,14 @@ __device__ __forceinline__ void colwise_from_tile(const StagedTile& t, int64_t R
   }
   if (kMX) {
     if (!(row < R && col < C)) return;  // R % 32 == 0: a 32-row MX block is all in or all out
+    const uint32_t round = mx_round(mode);
+    uint8_t* qcol = qT + col * R + row;
+    uint8_t* ecol = e8 + col * (R / 32) + row / 32;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int E = mx_exponent(unpack_amax(m, j), mode);
-      if ((rg & 3) == 0) e8[(col + j) * (R / 32) + row / 32] = static_cast<uint8_t>(E + 127);
-      st_v2(qT + (col + j) * R + row, column8_mul(v, j, pow2_neg(E)));
+      const MxScale sc = mx_scale(unpack_amax_bits(m, j), round);
+      if ((rg & 3) == 0) ecol[j * (R / 32)] = static_cast<uint8_t>(sc.e8);
+      st_v2(qcol + j * R, column8_mul(v, j, sc.mul));
     }
   } else {
     // Blockwise tiles are whole (R, C multiples of 128).  Lane j of each
@@ -431,17 +445,19 @@ __device__ __forceinline__ void rowwise_mx_from_tile(const StagedTile& t, int64_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = lane >> 4, l16 = lane & 15;
   const int64_t col = c0 + l16 * 8;
+  const int64_t rfirst = r0 + warp * 16 + h;  // rows rfirst + 2i
+  const uint32_t round = mx_round(mode);
+  uint8_t* qrow = q + rfirst * C + col;
+  uint8_t* erow = e8 + rfirst * (C / 32) + col / 32;
   uint4 v[8];
   read_rows(t, v);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int64_t r = r0 + warp * 16 + i * 2 + h;
     const uint32_t mm = shfl_absmax(shfl_absmax(absmax8(v[i]), 1), 2);
-    const float a = fmaxf(__uint_as_float((mm & 0x7FFFu) << 16), __uint_as_float(mm & 0x7FFF0000u));
-    if (r >= R || col >= C) continue;  // C % 32 == 0: a 32-column block is all in or all out
-    const int E = mx_exponent(a, mode);
-    st_v2(q + r * C + col, quant8_mul(v[i], pow2_neg(E)));
-    if ((l16 & 3) == 0) e8[r * (C / 32) + col / 32] = static_cast<uint8_t>(E + 127);
+    if (rfirst + 2 * i >= R || col >= C) continue;  // C % 32 == 0: a 32-column block is all in or all out
+    const MxScale sc = mx_scale(bf16_pair_max_bits(mm), round);
+    st_v2(qrow + 2 * i * C, quant8_mul(v[i], sc.mul));
+    if ((l16 & 3) == 0) erow[2 * i * (C / 32)] = static_cast<uint8_t>(sc.e8);
   }
 }
 
@@ -568,15 +584,15 @@ __global__ void __launch_bounds__(256) mx_quant_row_kernel(const uint16_t* __res
     const int64_t r = rbase + i;
     v[i] = (col_ok && r < R) ? ld_nc_v4(x + r * C + col) : make_uint4(0, 0, 0, 0);
   }
+  const uint32_t round = mx_round(mode);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int64_t r = rbase + i;
-    uint32_t mm = shfl_absmax(shfl_absmax(absmax8(v[i]), 1), 2);
-    const float a = fmaxf(__uint_as_float((mm & 0x7FFFu) << 16), __uint_as_float(mm & 0x7FFF0000u));
+    const uint32_t mm = shfl_absmax(shfl_absmax(absmax8(v[i]), 1), 2);
     if (!col_ok || r >= R) continue;
-    const int E = mx_exponent(a, mode);
-    st_v2(q + r * C + col, quant8_mul(v[i], pow2_neg(E)));
-    if ((lane & 3) == 0) e8[r * (C / 32) + col / 32] = static_cast<uint8_t>(E + 127);
+    const MxScale sc = mx_scale(bf16_pair_max_bits(mm), round);
+    st_v2(q + r * C + col, quant8_mul(v[i], sc.mul));
+    if ((lane & 3) == 0) e8[r * (C / 32) + col / 32] = static_cast<uint8_t>(sc.e8);
   }
 }
 
