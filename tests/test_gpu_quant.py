@@ -1,7 +1,8 @@
 """GPU parity of the quantizers: bit-exact e4m3 bytes and scale bits vs the oracle.
 
 Covers several tiles with ragged edges (MX), the edge cases of
-``gpu_util.adversarial_bf16``, both MX exponent modes, and the full-size dense
+``gpu_util.adversarial_bf16``, both MX exponent modes, every finite bf16
+value as a block max (1x128 and 1x32, rowwise and colwise), and the full-size dense
 linear workload (x[16384, 5120], W[8192, 5120], dy[16384, 8192]) and the
 full-size MXFP8 MoE tensors (x[16384, 5120], dy[16384, 8192] rowwise and
 colwise, the expert weights W[8, 8192, 5120] rowwise and 3D colwise),
@@ -106,6 +107,27 @@ def test_signed_zero_and_ties_on_device():
     assert np.all(s == 1.0)
 
 
+def test_1x128_every_bf16_block_max():
+    # The blockwise scale and the division over every finite bf16 block max
+    # (zero takes the 1e-12 floor), rowwise and -- on the transpose --
+    # colwise, through the separate and the fused kernels.
+    x = _every_bf16_block_max(50, width=128)
+    xT = x.t().contiguous()  # [128, 32640]
+    qo, so = oracle.quant_1x128_row(f32(x))
+    qTo, sTo = oracle.quant_1x128_col(f32(xT))
+    assert np.array_equal(qTo, qo) and np.array_equal(bits(sTo).reshape(-1), bits(so).reshape(-1))
+    q, s = run_row(x)
+    assert np.array_equal(q, qo) and np.array_equal(bits(s), bits(so))
+    qT, sT = run_col(xT)
+    assert np.array_equal(qT, qTo) and np.array_equal(bits(sT), bits(sTo))
+    xd = x.cuda()
+    q, s = B.alloc_quant_1x128_row(xd)
+    qT, sT = B.alloc_quant_1x128_col(xd)
+    B.fp8bw_quant_1x128_rowcol(xd, q, s, qT, sT)
+    B.fp8bw_sync_status()
+    assert np.array_equal(u8(q), qo) and np.array_equal(bits(s.cpu().numpy()), bits(so))
+
+
 # ---------------------------------------------------------------- MXFP8
 
 @pytest.mark.parametrize("mode", [B.MX_RCEIL, B.MX_FLOOR])
@@ -184,6 +206,49 @@ def test_mx_rowcol_3d_bit_exact(mode):
     qTo, eTo = oracle.mx_quant_3d_col(f32(w), mode)
     assert np.array_equal(q, qo) and np.array_equal(e8, eo)
     assert np.array_equal(qT, qTo) and np.array_equal(e8T, eTo)
+
+
+def _every_bf16_block_max(seed, width=32):
+    """[32640, width] bf16: row i's block max is the finite bf16 magnitude
+    with bits i (0x0000 .. 0x7F7F: zero, every subnormal and every normal),
+    the other elements bf16(max * u) with u uniform in [-1, 1]."""
+    amax = (np.arange(0, 0x7F80, dtype=np.uint32) << 16).view(np.float32)
+    u = np.random.default_rng(seed).uniform(-1.0, 1.0, size=(amax.size, width)).astype(np.float32)
+    x = amax[:, None] * u
+    x[:, 0] = amax
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    assert np.array_equal(np.abs(f32(xb)).max(axis=1), amax)
+    return xb
+
+
+@pytest.mark.parametrize("mode", [B.MX_RCEIL, B.MX_FLOOR])
+def test_mx_every_bf16_block_max(mode):
+    # The E8M0 exponent and 2^-E over every finite bf16 block max, through
+    # the rowwise and colwise MX kernels and the fused one, against the
+    # oracle's rule (reading 9, itself pinned by brute force in
+    # test_oracle_mx.py).
+    x = _every_bf16_block_max(40 + mode)
+    xT = x.t().contiguous()  # [32, 32640]: the same blocks down the columns
+    qo, eo = oracle.mx_quant_1x32_row(f32(x), mode)
+    qTo, eTo = oracle.mx_quant_1x32_col(f32(xT), mode)
+    assert np.array_equal(qTo, qo) and np.array_equal(eTo.reshape(-1), eo.reshape(-1))
+
+    xd = x.cuda()
+    q, e8 = B.alloc_mx_row(xd)
+    B.mxfp8_quant_1x32_row(xd, q, e8, mode)
+    B.fp8bw_sync_status()
+    assert np.array_equal(u8(q), qo) and np.array_equal(u8(e8), eo)
+
+    xTd = xT.cuda()
+    qT, e8T = B.alloc_mx_col(xTd)
+    B.mxfp8_quant_1x32_col(xTd, qT, e8T, mode)
+    B.fp8bw_sync_status()
+    assert np.array_equal(u8(qT), qTo) and np.array_equal(u8(e8T), eTo)
+
+    q, e8, qT, e8T = _mx_rowcol(x, mode)
+    assert np.array_equal(q, qo) and np.array_equal(e8, eo)
+    q, e8, qT, e8T = _mx_rowcol(xT, mode)
+    assert np.array_equal(qT[0], qTo) and np.array_equal(e8T[0], eTo)
 
 
 # ---------------------------------------------------------------- full size
