@@ -64,7 +64,7 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 
 class ClockSampler:
     """SM clock and clock-event reasons sampled on a thread while the timed
-    region runs: through the driver's NVML library (ctypes, every ~2 ms, so a
+    region runs: through NVML (ctypes, every ~2 ms, so a
     region of tens of milliseconds still gets many samples), or through
     `nvidia-smi -lms 50` where NVML cannot be loaded.  Reads only; changes no
     setting of the GPU."""
