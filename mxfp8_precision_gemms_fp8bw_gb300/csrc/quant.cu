@@ -12,6 +12,7 @@
 // whose columns it packs into e4m3 bytes, so every store is a coalesced
 // 8-byte vector.
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -33,15 +34,16 @@ namespace fp8bw {
 //   t = (A + round) >> 7,  round = 0x1F (RCEIL) or 0 (FLOOR),
 // is E + 135.  The clamp E >= -127 is t >= 8 (it also catches ef = 0); the
 // top clamp cannot bind (t <= 256).  The E8M0 byte E + 127 is t - 8 and the
-// scale 2^-E has biased exponent 262 - t, in [6, 254]: always a normal float.
+// scale 2^-E has biased exponent 262 - t, in [6, 254]: always a normal bf16
+// (and fp32), which the element scaling multiplies in as a bf16 operand.
 struct MxScale {
-  uint32_t e8;  // the E8M0 code E + 127
-  float mul;    // 2^-E
+  uint32_t e8;   // the E8M0 code E + 127
+  uint16_t mul;  // 2^-E as bf16 bits (biased exponent 262 - t, zero mantissa)
 };
 __device__ __forceinline__ uint32_t mx_round(int mode) { return mode == 0 ? 0x1Fu : 0u; }
 __device__ __forceinline__ MxScale mx_scale(uint32_t A, uint32_t round) {
   const uint32_t t = max((A + round) >> 7, 8u);
-  return MxScale{t - 8u, __uint_as_float((262u - t) << 23)};
+  return MxScale{t - 8u, static_cast<uint16_t>((262u - t) << 7)};
 }
 // Magnitude bits of the larger of the two bf16 values packed in `w` (the
 // sign bits may be anything).
@@ -102,10 +104,33 @@ __device__ __forceinline__ uint2 quant8_div(const uint4& v, float s, float ny) {
 }
 
 // Eight e4m3 codes of x * m (MX: m = 2^-E, an exact power of two).
-__device__ __forceinline__ uint2 quant8_mul(const uint4& v, float m) {
-  const float2 M = make_float2(m, m);
-  const float2 a = __fmul2_rn(pair_of_word(v.x), M), b = __fmul2_rn(pair_of_word(v.y), M);
-  const float2 c = __fmul2_rn(pair_of_word(v.z), M), d = __fmul2_rn(pair_of_word(v.w), M);
+// (lo, hi) of a packed bf16 pair times the bf16 power of two m, in fp32:
+// the product is exact (or rounds once, where it falls below the fp32
+// range, exactly as an fp32 multiply would), and adding -0 keeps the sign
+// of a zero product.
+__device__ __forceinline__ float2 bf16x2_times(uint32_t w, uint16_t m) {
+  float2 r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, lo, %3, %4;\n\tfma.rn.f32.bf16 %1, hi, %3, %4;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(w), "h"(m), "f"(-0.0f));
+  return r;
+}
+template <int kHi>
+__device__ __forceinline__ float bf16_half_times(uint32_t w, uint16_t m) {
+  float r;
+  if (kHi)
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tfma.rn.f32.bf16 %0, hi, %2, %3;\n\t}"
+        : "=f"(r) : "r"(w), "h"(m), "f"(-0.0f));
+  else
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tfma.rn.f32.bf16 %0, lo, %2, %3;\n\t}"
+        : "=f"(r) : "r"(w), "h"(m), "f"(-0.0f));
+  return r;
+}
+
+__device__ __forceinline__ uint2 quant8_mul(const uint4& v, uint16_t m) {
+  const float2 a = bf16x2_times(v.x, m), b = bf16x2_times(v.y, m);
+  const float2 c = bf16x2_times(v.z, m), d = bf16x2_times(v.w, m);
   return make_uint2(__byte_perm(cvt_e4m3x2(a.x, a.y), cvt_e4m3x2(b.x, b.y), 0x5410),
                     __byte_perm(cvt_e4m3x2(c.x, c.y), cvt_e4m3x2(d.x, d.y), 0x5410));
 }
@@ -327,12 +352,16 @@ __device__ __forceinline__ uint2 column8_div(const uint4 (&v)[8], int j, float s
   return make_uint2(e4m3x4_from_neg(a, b), e4m3x4_from_neg(c, d));
 }
 
-__device__ __forceinline__ uint2 column8_mul(const uint4 (&v)[8], int j, float m) {
-  const float2 M = make_float2(m, m);
-  const float2 a = __fmul2_rn(make_float2(elem8(v[0], j), elem8(v[1], j)), M);
-  const float2 b = __fmul2_rn(make_float2(elem8(v[2], j), elem8(v[3], j)), M);
-  const float2 c = __fmul2_rn(make_float2(elem8(v[4], j), elem8(v[5], j)), M);
-  const float2 d = __fmul2_rn(make_float2(elem8(v[6], j), elem8(v[7], j)), M);
+template <int kJ>
+__device__ __forceinline__ float elem8_times(const uint4& v, uint16_t m) {
+  return bf16_half_times<kJ & 1>(word(v, kJ >> 1), m);
+}
+template <int kJ>
+__device__ __forceinline__ uint2 column8_mul(const uint4 (&v)[8], uint16_t m) {
+  const float2 a = make_float2(elem8_times<kJ>(v[0], m), elem8_times<kJ>(v[1], m));
+  const float2 b = make_float2(elem8_times<kJ>(v[2], m), elem8_times<kJ>(v[3], m));
+  const float2 c = make_float2(elem8_times<kJ>(v[4], m), elem8_times<kJ>(v[5], m));
+  const float2 d = make_float2(elem8_times<kJ>(v[6], m), elem8_times<kJ>(v[7], m));
   return make_uint2(__byte_perm(cvt_e4m3x2(a.x, a.y), cvt_e4m3x2(b.x, b.y), 0x5410),
                     __byte_perm(cvt_e4m3x2(c.x, c.y), cvt_e4m3x2(d.x, d.y), 0x5410));
 }
@@ -381,12 +410,20 @@ __device__ __forceinline__ void colwise_from_tile(const StagedTile& t, int64_t R
     const uint32_t round = mx_round(mode);
     uint8_t* qcol = qT + col * R + row;
     uint8_t* ecol = e8 + col * (R / 32) + row / 32;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    auto column = [&](auto J) {
+      constexpr int j = decltype(J)::value;
       const MxScale sc = mx_scale(unpack_amax_bits(m, j), round);
       if ((rg & 3) == 0) ecol[j * (R / 32)] = static_cast<uint8_t>(sc.e8);
-      st_v2(qcol + j * R, column8_mul(v, j, sc.mul));
-    }
+      st_v2(qcol + j * R, column8_mul<j>(v, sc.mul));
+    };
+    column(std::integral_constant<int, 0>{});
+    column(std::integral_constant<int, 1>{});
+    column(std::integral_constant<int, 2>{});
+    column(std::integral_constant<int, 3>{});
+    column(std::integral_constant<int, 4>{});
+    column(std::integral_constant<int, 5>{});
+    column(std::integral_constant<int, 6>{});
+    column(std::integral_constant<int, 7>{});
   } else {
     // Blockwise tiles are whole (R, C multiples of 128).  Lane j of each
     // half-warp derives column j's scale; shuffles hand it to the others.
