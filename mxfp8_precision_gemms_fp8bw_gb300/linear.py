@@ -351,8 +351,11 @@ class ToyFFNStep:
     Inputs: x [M, dim], w1, w2 [hidden, dim], wo [dim, hidden], dy [M, dim]
     bf16.  x is quantized once (rowwise and colwise in one pass) for both
     up-projections.  The silu * mul activation and its derivative are the
-    model's own elementwise code, run as bf16/fp32 torch ops between the
-    library calls (not part of the library).  ``kernels`` lists the step's
+    model's own elementwise code (not part of the library), run as the bf16
+    torch ops that autograd runs for ``silu(h1) * h2``: silu(h1) and the
+    product are each rounded to bf16; backward, g = da * h2, dh1 =
+    silu_backward(g, h1) and dh2 = da * silu(h1), each rounded to bf16.
+    ``kernels`` lists the step's
     calls in order as (name, callable) pairs for per-call timing; names of
     library GEMMs start with "gemm".
     """
@@ -379,6 +382,7 @@ class ToyFFNStep:
             act(M, hidden), act(M, hidden)
         self.w1q, self.w2q, self.woq = wt(hidden, dim), wt(hidden, dim), wt(dim, hidden)
         self.h1, self.h2, self.a = e((M, hidden), bf), e((M, hidden), bf), e((M, hidden), bf)
+        self.s1, self.g = e((M, hidden), bf), e((M, hidden), bf)  # silu(h1) (kept for backward), da * h2
         self.out, self.da, self.dh1, self.dh2 = e((M, dim), bf), e((M, hidden), bf), e((M, hidden), bf), \
             e((M, hidden), bf)
         self.dx1, self.dx2, self.dx = e((M, dim), bf), e((M, dim), bf), e((M, dim), bf)
@@ -392,14 +396,13 @@ class ToyFFNStep:
         return lambda: B.fp8bw_quant_1x128_rowcol(src, a["q"], a["s"], a["qT"], a["sT"], stream)
 
     def _act(self):
-        h1 = self.h1.float()
-        self.a.copy_((h1 * torch.sigmoid(h1) * self.h2.float()).bfloat16())
+        torch.ops.aten.silu.out(self.h1, out=self.s1)
+        torch.mul(self.s1, self.h2, out=self.a)
 
     def _act_grad(self):
-        h1, h2, da = self.h1.float(), self.h2.float(), self.da.float()
-        sig = torch.sigmoid(h1)
-        self.dh1.copy_((da * h2 * (sig * (1 + h1 * (1 - sig)))).bfloat16())
-        self.dh2.copy_((da * h1 * sig).bfloat16())
+        torch.mul(self.da, self.h2, out=self.g)
+        torch.ops.aten.silu_backward.grad_input(self.g, self.h1, grad_input=self.dh1)
+        torch.mul(self.da, self.s1, out=self.dh2)
 
     def kernels(self, x, w1, w2, wo, dy, stream=None):
         xa, aa, dya, d1, d2 = self.xa, self.aa, self.dya, self.dh1a, self.dh2a

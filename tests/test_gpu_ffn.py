@@ -17,8 +17,8 @@ workloads (M = 128000) whose wgrad contracts over 128000 tokens.
   dx 19.3, d_w1 16.8, d_w2 25.6, d_out_proj 24.8 dB): each 128-token block of
   the colwise (token-blocked) operands holds an outlier row 10-100x larger than
   the rest, which coarsens every other row of the block.  The silu * mul
-  activation between the GEMMs is the model's own code (bf16 torch ops), as in
-  the ToyModel.
+  activation between the GEMMs is the model's own code, the bf16 torch ops
+  autograd runs for silu(h1) * h2 (each op's result rounded to bf16).
 """
 import numpy as np
 import pytest
@@ -123,11 +123,13 @@ def _oracle_chain(t):
 
     h1, h2 = _bf(fwd(x, w1)), _bf(fwd(x, w2))
     s = 1.0 / (1.0 + np.exp(-h1.astype(np.float64)))
-    a = _bf(h1 * s * h2)
+    s1 = _bf(h1 * s)  # silu(h1) in bf16
+    a = _bf(s1 * h2)
     out = fwd(a, wo)
     da, d_wo = bwd(dy, a, wo)
     da = _bf(da)
-    dh1, dh2 = _bf(da * h2 * (s * (1 + h1 * (1 - s)))), _bf(da * h1 * s)
+    g = _bf(da * h2)  # the gradient reaching silu's output
+    dh1, dh2 = _bf(g * (s * (1 + h1 * (1 - s)))), _bf(da * s1)
     dx1, d_w1 = bwd(dh1, x, w1)
     dx2, d_w2 = bwd(dh2, x, w2)
     return {"out": out, "dx": dx1 + dx2, "d_w1": d_w1, "d_w2": d_w2, "d_out_proj": d_wo}
