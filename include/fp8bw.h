@@ -194,8 +194,9 @@ int fp8bw_gemm_wgrad_ws(const uint8_t* dyqT, const float* dysT, const uint8_t* x
                         size_t workspace_bytes, void* stream);
 
 /* Bytes of workspace fp8bw_gemm_wgrad_ws uses for these dims on the current
- * device (0 when its tiles fill whole rounds of SMs, or when the dims are
- * invalid or no device is present).  Enqueues no work. */
+ * device: 0 when splitting the last round of tiles would not pay (for one,
+ * when the tiles fill whole rounds of SMs), or when the dims are invalid or
+ * no device is present.  Enqueues no work. */
 size_t fp8bw_gemm_wgrad_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /* dW += dy^T x with dW in fp32: the wgrad GEMM above, its tile added to the
