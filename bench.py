@@ -215,7 +215,9 @@ def oracle_sample(rows: int, w_rows: int):
     quantization of the step on that sample (rowwise and colwise for x and dy,
     128x128 for W) and the three GEMMs restricted to it (dgrad and wgrad
     contract over the sampled features / tokens only).
-    Returns (seconds, gemm flops, threads)."""
+    Returns (seconds, gemm flops, threads, quantizer seconds, quantizer
+    algorithmic bytes): the five quantizations are also timed on their own,
+    since quantizers are reported in GB/s apart from the GEMMs."""
     import oracle
     from mxfp8_precision_gemms_fp8bw_gb300 import inputs
 
@@ -223,16 +225,28 @@ def oracle_sample(rows: int, w_rows: int):
     x = inputs.bf16_to_f32_numpy(t.x[:rows])
     w = inputs.bf16_to_f32_numpy(t.w[:w_rows])
     dy = inputs.bf16_to_f32_numpy(t.dy[:rows, :w_rows])
+    qsecs = 0.0
+
+    def quant(fn, a):
+        nonlocal qsecs
+        q0 = time.perf_counter()
+        out = fn(a)
+        qsecs += time.perf_counter() - q0
+        return out
+
     t0 = time.perf_counter()
-    xq, xs = oracle.quant_1x128_row(x)
-    wq, _, ws = oracle.quant_128x128(w)
+    xq, xs = quant(oracle.quant_1x128_row, x)
+    wq, _, ws = quant(oracle.quant_128x128, w)
     y = oracle.gemm_fwd(xq, xs, wq, ws)
-    dyq, dys = oracle.quant_1x128_row(dy)
+    dyq, dys = quant(oracle.quant_1x128_row, dy)
     dx = oracle.gemm_dgrad(dyq, dys, wq, ws)
-    dyqT, dysT = oracle.quant_1x128_col(dy)
-    xqT, xsT = oracle.quant_1x128_col(x)
+    dyqT, dysT = quant(oracle.quant_1x128_col, dy)
+    xqT, xsT = quant(oracle.quant_1x128_col, x)
     dW = oracle.gemm_wgrad(dyqT, dysT, xqT, xsT)
     secs = time.perf_counter() - t0
+    # Algorithmic bytes of the five calls: bf16 read, e4m3 written, fp32
+    # scales (one per 128 elements for 1x128, one per 128x128 tile for W).
+    qbytes = 2 * (rows * K + rows * w_rows) * (3 + 4 / 128) + w_rows * K * (3 + 4 / (128 * 128))
     assert y.shape == (rows, w_rows) and dx.shape == (rows, K) and dW.shape == (w_rows, K)
     threads = os.cpu_count() or 1
     try:
@@ -242,7 +256,7 @@ def oracle_sample(rows: int, w_rows: int):
             threads = max(i.get("num_threads", 1) for i in info)
     except ImportError:
         pass
-    return secs, 6 * rows * w_rows * K, threads
+    return secs, 6 * rows * w_rows * K, threads, qsecs, qbytes
 
 
 def sample_desc(rows, w_rows):
@@ -271,7 +285,7 @@ def run_reference(args, world, rank):
         oracle_sample(rows, w_rows)
     secs_all = []
     for _ in range(args.steps):
-        secs, flops, threads = oracle_sample(rows, w_rows)
+        secs, flops, threads, _, _ = oracle_sample(rows, w_rows)
         secs_all.append(secs)
         vals.append(flops / secs / 1e12)
     value = statistics.median(vals)
@@ -382,9 +396,11 @@ def run_ours(args, world, rank, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rows, w_rows = CPU_SAMPLE
-        secs, flops, threads = oracle_sample(rows, w_rows)
+        secs, flops, threads, qsecs, qbytes = oracle_sample(rows, w_rows)
         cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": sample_desc(rows, w_rows), "seconds": round(secs, 2)}
+               "sample": sample_desc(rows, w_rows), "seconds": round(secs, 2),
+               "gemm_tflops": round(flops / (secs - qsecs) / 1e12, 4),
+               "quant_gbs": round(qbytes / qsecs / 1e9, 3)}
 
     if rank == 0:
         line = {
